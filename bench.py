@@ -1,0 +1,515 @@
+"""Benchmark of the paged-KV attention hot path on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+
+One step = one pass of the hot path over the 128-sequence Qwen3-0.6B-like
+decode batch (16 q / 8 KV heads, head_dim 128, contexts U[100, 1024], 256-token
+blocks in a 1024-block pool): pkv_store_kvcache of the new K/V row of every
+sequence, then pkv_decode_attention (split kernel + log-sum-exp combine).
+The metric is KV GB/s (algorithmic bytes / step time) with decode tokens/s per
+layer beside it.  The long-context decode, prefix-sharing decode and chunked
+prefill workloads are measured too and reported under "other_workloads".
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
+cudaDeviceSynchronize; L2 (126 MB) is flushed before every step by a 256 MiB
+write and each step is timed alone with CUDA events on the launching stream.
+A second timed pass with the library's kernel profiler on gives per-kernel
+durations for the roofline.  Under torchrun each rank runs an independent
+replica on its own GPU (no collective on the data path); value = bytes of all
+ranks / max over ranks of the time.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of each step) and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_493_b300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s (% of HBM peak) and decode tokens/s/layer"
+MAIN_WORKLOAD = "qwen_decode_b128"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_setup():
+    """(rank, world, local_rank); initialises torch.distributed when WORLD_SIZE > 1."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float) -> float:
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return float(x)
+
+
+def replica_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch: weak scaling over independent replicas."""
+    return base + 7919 * rank
+
+
+# ----------------------------------------------------------------------------- work model
+def decode_kv_bytes(case) -> int:
+    c = case.cache
+    hkv, d = int(c.k_cache.shape[2]), int(c.k_cache.shape[3])
+    return int(c.context_lens.sum()) * hkv * d * 2 * 2
+
+
+def decode_step_bytes(case) -> dict:
+    """Algorithmic bytes of one decode step: every cached K/V row read once, q
+    read, out written, new rows read and written, metadata read."""
+    kv = decode_kv_bytes(case)
+    q = case.q.numel() * 2
+    new = (case.k_new.numel() + case.v_new.numel()) * 2
+    meta = (case.cache.block_tables.numel() + case.cache.context_lens.numel() +
+            case.slot_mapping.numel()) * 4
+    return {"kv": kv, "split_kernel": kv + q + meta, "step": kv + 2 * q + 2 * new + meta}
+
+
+def unique_kv_bytes(case) -> int:
+    """K/V bytes of distinct physical token slots (shared prefix blocks counted once)."""
+    c = case.cache
+    hkv, d = int(c.k_cache.shape[2]), int(c.k_cache.shape[3])
+    per_block = {}
+    for s, ctx in enumerate(c.context_lens.tolist()):
+        row = c.block_tables[s].tolist()
+        for b in range((ctx + 255) // 256):
+            n = min(256, ctx - b * 256)
+            per_block[row[b]] = max(per_block.get(row[b], 0), n)
+    return sum(per_block.values()) * hkv * d * 2 * 2
+
+
+def prefill_flops(case) -> int:
+    c = case.cache
+    hq, d = int(case.q.shape[1]), int(case.q.shape[2])
+    cu = case.cu_seqlens_q.tolist()
+    total = 0
+    for s, ctx in enumerate(c.context_lens.tolist()):
+        lq = cu[s + 1] - cu[s]
+        # query i sees ctx - lq + i + 1 keys; QK^T and PV are 2 * d flops per key each
+        keys = lq * (ctx - lq) + lq * (lq + 1) // 2
+        total += keys * hq * d * 4
+    return total
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, max_mhz_hint: float) -> dict:
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz_hint, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax) if smax else max_mhz_hint,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def to_dev(t):
+    return t.to("cuda", non_blocking=False)
+
+
+class Flusher:
+    """Writes 256 MiB (> 2x the 126 MB L2) to evict cached lines between steps."""
+
+    def __init__(self):
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.k = 0
+
+    def __call__(self):
+        self.k = (self.k + 1) & 0xFF
+        self.buf.fill_(self.k)
+
+
+def time_steps(step, steps: int, flush: Flusher):
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, wall
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class DecodeBench:
+    def __init__(self, case, pkv):
+        self.case, self.pkv = case, pkv
+        c = case.cache
+        self.kc, self.vc = to_dev(c.k_cache), to_dev(c.v_cache)
+        self.bt, self.cl = to_dev(c.block_tables), to_dev(c.context_lens)
+        self.q, self.kn, self.vn = to_dev(case.q), to_dev(case.k_new), to_dev(case.v_new)
+        self.sm = to_dev(case.slot_mapping)
+        self.out = torch.empty_like(self.q)
+        pkv.pkv_reserve_workspace(case.num_seqs, int(case.q.shape[1]), int(case.q.shape[2]),
+                                  int(c.block_tables.shape[1]))
+
+    def step(self):
+        p = self.pkv
+        p.pkv_store_kvcache(self.kn, self.vn, self.sm, self.kc, self.vc)
+        p.pkv_decode_attention(self.q, self.kc, self.vc, self.bt, self.cl, self.case.scale, self.out)
+
+    def e2e_setup(self):
+        c = self.case
+        pin = lambda t: t.clone().pin_memory()  # noqa: E731
+        self.h_in = [pin(c.q), pin(c.k_new), pin(c.v_new), pin(c.slot_mapping),
+                     pin(c.cache.block_tables), pin(c.cache.context_lens)]
+        self.d_in = [torch.empty_like(t, device="cuda") for t in self.h_in]
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        d2h = self.h_out.numel() * self.h_out.element_size()
+        return h2d, d2h
+
+    def e2e_step(self):
+        p = self.pkv
+        for h, d in zip(self.h_in, self.d_in):
+            d.copy_(h, non_blocking=True)
+        q, kn, vn, sm, bt, cl = self.d_in
+        p.pkv_store_kvcache(kn, vn, sm, self.kc, self.vc)
+        p.pkv_decode_attention(q, self.kc, self.vc, bt, cl, self.case.scale, self.out)
+        self.h_out.copy_(self.out, non_blocking=True)
+
+
+def kernel_times(pkv, step, steps, flush, names):
+    pkv.pkv_profiler_reset()
+    pkv.pkv_profiler_enable(True)
+    try:
+        time_steps(step, steps, flush)
+        res = {n: pkv.pkv_profiler_read(n) for n in names}
+    finally:
+        pkv.pkv_profiler_enable(False)
+        pkv.pkv_profiler_reset()
+    return res
+
+
+def run_gpu(args, rank, world, local):
+    import paged_kv_cache_493_b300 as pkv
+    from paged_kv_cache_493_b300 import _build
+    _build.build()
+    pkv.load_library()
+    torch.cuda.set_device(local)
+    peaks, peak_src = load_peaks()
+    flush = Flusher()
+
+    case = W.qwen_decode(seed=replica_seed(1002, rank))
+    bytes_ = decode_step_bytes(case)
+    bench = DecodeBench(case, pkv)
+    for _ in range(args.warmup):
+        bench.step()
+    torch.cuda.synchronize()
+
+    with ClockSampler(local) as clk:
+        per, wall = time_steps(bench.step, args.steps, flush)
+        names = ["store_kvcache", "decode_split", "decode_combine"]
+        kt = kernel_times(pkv, bench.step, args.steps, flush, names)
+    step_ms = reduce_max(sum(per) / len(per))
+    value = world * bytes_["step"] / (step_ms * 1e-3) / 1e9
+    split_ms = kt["decode_split"][0] / max(kt["decode_split"][1], 1)
+    achieved = bytes_["split_kernel"] / (split_ms * 1e-3) / 1e9
+    launches_per_step = sum(n for _, n in kt.values()) / args.steps
+
+    # End to end through the C ABI from pinned host buffers.
+    h2d, d2h = bench.e2e_setup()
+    for _ in range(args.warmup):
+        bench.e2e_step()
+    e2e_per, _ = time_steps(bench.e2e_step, args.steps, flush)
+    e2e_ms = reduce_max(sum(e2e_per) / len(e2e_per))
+    torch.cuda.synchronize()
+    e2e_ok = torch.equal(bench.h_out.to("cuda"), bench.out)
+
+    other = {}
+    if not args.only_main:
+        other = other_workloads(pkv, args, rank, flush, peaks)
+
+    code, site = pkv.pkv_get_device_error()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": MAIN_WORKLOAD, "num_seqs": case.num_seqs, "context_lens": "U[100,1024] seeded",
+            "mean_context": round(float(case.cache.context_lens.float().mean()), 1),
+            "num_q_heads": 16, "num_kv_heads": 8, "head_dim": 128, "block_size": 256,
+            "num_blocks": case.cache.num_blocks, "step": "store_kvcache + decode (split + combine)",
+            "l2": "flushed before every step (256 MiB write), step timed alone",
+            "parallelism": f"replicas{world}",
+        },
+        "tokens_per_s_per_layer": round(world * case.num_seqs / (step_ms * 1e-3), 1),
+        "kv_gbs": round(world * bytes_["kv"] / (step_ms * 1e-3) / 1e9, 2),
+        "frac_of_hbm_peak": round(value / world / peaks["hbm_gbs"], 4),
+        "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
+        "wall_s_timed_region": round(wall, 4),
+        "roofline": {
+            "kernel": "decode_split",
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peaks["hbm_gbs"],
+            "peak_source": f"{peak_src} hbm_gbs (burst copy)",
+            "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": None,
+            "algorithmic_bytes_per_launch": bytes_["split_kernel"],
+            "avg_launch_ms": round(split_ms, 5),
+            "kernel_ms": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},
+        },
+        "e2e": {"value": round(world * bytes_["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "output_matches_device": bool(e2e_ok)},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "clocks": clk.summary(2032.0),
+        "device_error": code,
+    }
+    if rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(case, bytes_)
+    if other:
+        line["other_workloads"] = other
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def other_workloads(pkv, args, rank, flush, peaks):
+    res = {}
+    steps = max(3, min(args.steps, 10))
+    # Long-context and prefix-sharing decode.
+    for name, make in (("long_decode_32k", W.long_decode), ("prefix_decode_b64", W.prefix_decode)):
+        case = make(seed=replica_seed(1003 if name.startswith("long") else 1004, rank))
+        b = decode_step_bytes(case)
+        bench = DecodeBench(case, pkv)
+        for _ in range(3):
+            bench.step()
+        kt = kernel_times(pkv, bench.step, steps, flush, ["decode_split", "decode_combine"])
+        per, _ = time_steps(bench.step, steps, flush)
+        ms = sum(per) / len(per)
+        dec_ms = sum(v[0] for v in kt.values()) / steps
+        entry = {"step_ms": round(ms, 5), "decode_ms": round(dec_ms, 5),
+                 "kv_bytes": b["kv"], "kv_gbs": round(b["kv"] / (dec_ms * 1e-3) / 1e9, 2),
+                 "frac_of_hbm_peak": round(b["kv"] / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                 "tokens_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1)}
+        if name.startswith("prefix"):
+            u = unique_kv_bytes(case)
+            entry["unique_kv_bytes"] = u
+            entry["unique_kv_gbs"] = round(u / (dec_ms * 1e-3) / 1e9, 2)
+            entry["unique_frac_of_hbm_peak"] = round(u / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+        res[name] = entry
+        del bench
+        torch.cuda.empty_cache()
+    # Chunked prefill.
+    case = W.chunked_prefill(seed=replica_seed(1005, rank))
+    c = case.cache
+    kc, vc, bt, cl = to_dev(c.k_cache), to_dev(c.v_cache), to_dev(c.block_tables), to_dev(c.context_lens)
+    q, kn, vn, sm = to_dev(case.q), to_dev(case.k_new), to_dev(case.v_new), to_dev(case.slot_mapping)
+    cu = to_dev(case.cu_seqlens_q)
+    out = torch.empty_like(q)
+
+    def pstep():
+        pkv.pkv_store_kvcache(kn, vn, sm, kc, vc)
+        pkv.pkv_prefill_attention(q, kc, vc, bt, cu, cl, case.scale, out)
+
+    for _ in range(3):
+        pstep()
+    kt = kernel_times(pkv, pstep, steps, flush, ["store_kvcache", "prefill"])
+    per, _ = time_steps(pstep, steps, flush)
+    flops = prefill_flops(case)
+    pre_ms = kt["prefill"][0] / max(kt["prefill"][1], 1)
+    st_ms = kt["store_kvcache"][0] / max(kt["store_kvcache"][1], 1)
+    store_bytes = int((case.slot_mapping >= 0).sum()) * 8 * 128 * 2 * 2 * 2
+    tf = flops / (pre_ms * 1e-3) / 1e12
+    res["chunked_prefill_8x512"] = {
+        "step_ms": round(sum(per) / len(per), 5), "prefill_ms": round(pre_ms, 5), "flops": flops,
+        "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+        "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+        "store_ms": round(st_ms, 5), "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
+    return res
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_step_sample(case, seqs):
+    """store + decode of the listed sequences on the CPU oracle; returns KV bytes processed."""
+    import oracle
+    c = case.cache
+    sel = torch.tensor(seqs, dtype=torch.long)
+    kc, vc = oracle.store_kvcache(case.k_new[sel], case.v_new[sel], case.slot_mapping[sel],
+                                  c.k_cache, c.v_cache)
+    oracle.decode(case.q[sel], kc, vc, c.block_tables[sel], c.context_lens[sel], case.scale)
+    hkv, d = int(c.k_cache.shape[2]), int(c.k_cache.shape[3])
+    return int(c.context_lens[sel].sum()) * hkv * d * 4
+
+
+def cpu_baseline(case, bytes_, budget_s: float = 15.0):
+    """The oracle as it stands (single thread, fp64) on a bounded sample."""
+    n = case.num_seqs
+    seqs, done, elapsed = [], 0, 0.0
+    order = list(range(n))
+    t0 = time.perf_counter()
+    kv = 0
+    i = 0
+    while i < n and time.perf_counter() - t0 < budget_s:
+        chunk = order[i:i + 16]
+        kv += oracle_step_sample(case, chunk)
+        i += len(chunk)
+    elapsed = time.perf_counter() - t0
+    return {"value": round(kv / elapsed / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"store + decode of {i} of {n} sequences (all heads), {elapsed:.1f} s, "
+                      f"fp64 single-threaded C"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    case = W.qwen_decode(seed=1002)
+    per_step = 8  # sequences per step: a bounded sample of the workload
+    n = case.num_seqs
+    for i in range(args.warmup):
+        oracle_step_sample(case, [(i * per_step + j) % n for j in range(per_step)])
+    times, kv = [], 0
+    for i in range(args.steps):
+        seqs = [(i * per_step + j) % n for j in range(per_step)]
+        t0 = time.perf_counter()
+        kv += oracle_step_sample(case, seqs)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = kv / total / 1e9
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": MAIN_WORKLOAD, "num_seqs": n, "num_q_heads": 16, "num_kv_heads": 8,
+                   "head_dim": 128, "block_size": 256, "num_blocks": case.cache.num_blocks,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: store + decode of {per_step} of {n} sequences"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "pkv":
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local)
+    finally:
+        if torch.distributed.is_available() and torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

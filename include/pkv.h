@@ -1,0 +1,217 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a paged KV cache on one B300
+ * (sm_103a) GPU.
+ *
+ * The cache is cut into fixed blocks of 256 token slots (tuning guide
+ * "Nano-vLLM性能调优实战", §1.1 KV缓存块配置: kvcache_block_size 256).  Each
+ * sequence reaches its physically scattered blocks through a block table,
+ * and sequences that share a prefix point at the same physical blocks
+ * (ocdem.com nano-vllm article, §2.1 "基石PagedAttention 与 vLLM 的精髓").
+ * Three calls make up the hot path of one attention layer (tuning guide
+ * §2.2 缓存复用策略: a store_kvcache kernel writes new rows, attention then
+ * reads the cache, variable-length batches allowed):
+ *
+ *   pkv_store_kvcache      scatter of new K/V rows into cache slots;
+ *   pkv_decode_attention   one query token per sequence over its cache
+ *                          (split-K over the context, then a log-sum-exp
+ *                          combine);
+ *   pkv_prefill_attention  a chunk of query tokens per sequence over its
+ *                          cached prefix plus the chunk itself, causal.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor arguments are DEVICE pointers on the current CUDA device,
+ *   owned by the caller.  The library never frees them and keeps no
+ *   reference after the call returns.  Base pointers must be 16-byte
+ *   aligned and row strides (given in elements) must keep every row 16-byte
+ *   aligned.
+ * - bf16 is IEEE bfloat16 (the upper half of a binary32).  Index arrays are
+ *   int32.
+ * - Cache layout: k_cache and v_cache are bf16
+ *   [num_blocks][256][num_kv_heads][head_dim], contiguous.  Token slot
+ *   s = block_id * 256 + offset is the row k_cache + s * num_kv_heads * head_dim.
+ * - block_tables is int32 [num_seqs][max_blocks_per_seq], contiguous; entry
+ *   (s, i) is the physical block of logical block i of sequence s.  Entries
+ *   past ceil(context_lens[s] / 256) are never read (pad them with -1).
+ * - context_lens[s] counts every cached token of sequence s, including the
+ *   ones stored by this step's pkv_store_kvcache.
+ * - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * - Supported: head_dim 64 or 128; num_q_heads a multiple of num_kv_heads
+ *   with group size 1, 2, 4, 8 or 16.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream) and returns a pkv_status.  Shape, alignment and
+ *   pointer checks run on the host before any launch; a failed check
+ *   launches nothing.  Values that live on the device (block ids, slots,
+ *   lengths) are checked by the kernels: an out-of-range value is skipped
+ *   (its output row is written as zeros), never dereferenced, and recorded
+ *   in a per-device error word that pkv_get_device_error reads.
+ * - There is no CPU fallback: without a usable sm_103a device every call
+ *   returns PKV_ERR_CUDA.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* pkv_stream_t; /* a cudaStream_t */
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* null pointer, negative size, inconsistent shapes */
+  PKV_ERR_UNSUPPORTED = 2,  /* head_dim, group size or alignment not supported */
+  PKV_ERR_CUDA = 3,         /* a CUDA runtime call failed (no device, launch error) */
+  PKV_ERR_DEVICE_CHECK = 4, /* a kernel found an out-of-range block id, slot or length */
+  PKV_ERR_TIMEOUT = 5,      /* a bounded wait inside a kernel expired */
+  PKV_ERR_NO_MEMORY = 6     /* the library could not allocate its workspace */
+} pkv_status;
+
+#define PKV_BLOCK_SIZE 256
+
+/*
+ * pkv_store_kvcache -- write new K/V rows into their cache slots.
+ * (tuning guide §2.2: store_kvcache; ocdem.com article §2.1: slots live in
+ * fixed-size blocks)
+ *
+ *   k, v          bf16 [num_tokens][*]: row i starts at k + i * k_row_stride
+ *                 (v + i * v_row_stride) and holds num_kv_heads * head_dim
+ *                 contiguous values (heads outer, head_dim inner).
+ *   slot_mapping  int32 [num_tokens]: destination slot of row i, or -1 to
+ *                 skip the row.  Any other value outside
+ *                 [0, num_blocks * 256) is skipped and reported as
+ *                 PKV_ERR_DEVICE_CHECK.  Two rows with the same slot: which
+ *                 one lands is unspecified.
+ *   k_cache, v_cache  bf16 [num_blocks][256][num_kv_heads][head_dim],
+ *                 updated in place.  Slots that no row maps to are untouched.
+ *
+ * The copy is bit-exact.  num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
+                             int64_t v_row_stride, const int32_t* slot_mapping,
+                             int64_t num_tokens, void* k_cache, void* v_cache,
+                             int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                             pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention -- one query token per sequence attends to all
+ * context_lens[s] cached tokens of its sequence (intelliparadigm.com
+ * Nano-vLLM article, §7.1 增量解码; tuning guide §2.2 flash_attn_with_kvcache).
+ *
+ *   q             bf16 [num_seqs][*]: the query of sequence s starts at
+ *                 q + s * q_row_stride and holds num_q_heads * head_dim values.
+ *   k_cache, v_cache, num_blocks   the cache, as above.
+ *   block_tables  int32 [num_seqs][max_blocks_per_seq].
+ *   context_lens  int32 [num_seqs], 0 <= context_lens[s] <= 256 * max_blocks_per_seq.
+ *   scale         softmax scale applied to q.k (typically 1/sqrt(head_dim)).
+ *   out           bf16 [num_seqs][num_q_heads][head_dim], contiguous; written.
+ *
+ *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K[s][t][g(h)]) * V[s][t][g(h)]
+ *
+ * with fp32 accumulation and bf16 (round to nearest even) output.  A
+ * sequence with context 0 gets a zero output.  The context is split into
+ * ranges processed in parallel (flash decoding; the number of ranges per
+ * sequence is chosen from the batch shape and capped by pkv_set_max_splits)
+ * and the partial results are merged by a log-sum-exp combine.  The partials
+ * live in a library-owned workspace on the current device, allocated (and
+ * grown) with cudaMalloc on first need; call pkv_reserve_workspace before
+ * capturing this call in a CUDA graph.  Calls on different streams that
+ * overlap share that workspace and must be serialised by the caller.
+ */
+pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
+                                const void* v_cache, int64_t num_blocks,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t num_seqs,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                float scale, void* out, pkv_stream_t stream);
+
+/*
+ * pkv_prefill_attention -- chunked causal prefill over cached blocks
+ * (tuning guide §3.2: chunks bounded by max_num_batched_tokens; §2.2:
+ * variable-length batches; intelliparadigm.com article §7.1 预填充阶段).
+ *
+ *   q             bf16 [total_q][*]: query row r starts at q + r * q_row_stride
+ *                 and holds num_q_heads * head_dim values.  Sequence s owns rows
+ *                 cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1 (its chunk, Lq rows).
+ *                 q_row_stride * 2 bytes must be a multiple of 16.
+ *   cu_seqlens_q  int32 [num_seqs + 1], non-decreasing, cu_seqlens_q[0] = 0,
+ *                 cu_seqlens_q[num_seqs] = total_q.
+ *   context_lens  int32 [num_seqs]: C = cached tokens including the chunk
+ *                 (the chunk's K/V must already be stored); Lq <= C.
+ *   out           bf16 [total_q][num_q_heads][head_dim], contiguous; written.
+ *
+ * Query i of the chunk sits at position C - Lq + i and attends to keys
+ * 0 .. C - Lq + i (causal, aligned to the end of the context).  QK^T and PV
+ * run on the tcgen05 tensor cores with fp32 accumulation in tensor memory;
+ * P is rounded to bf16 before PV.  Output is bf16.
+ */
+pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void* k_cache,
+                                 const void* v_cache, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                 int32_t num_seqs, int64_t total_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
+                                 pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Helpers
+ * --------------------------------------------------------------------- */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* pkv_status_string(pkv_status status);
+
+/* Library version string, e.g. "pkv 0.1.0 sm_103a". */
+const char* pkv_version(void);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error
+ * word.  *code receives PKV_OK or the first PKV_ERR_DEVICE_CHECK /
+ * PKV_ERR_TIMEOUT recorded since the last read; *info (may be NULL) an
+ * internal site code for diagnostics.  Returns PKV_ERR_CUDA if the
+ * synchronisation failed.
+ */
+pkv_status pkv_get_device_error(pkv_stream_t stream, int32_t* code, int32_t* info);
+
+/*
+ * Cap the number of context ranges one sequence is split into by
+ * pkv_decode_attention (0 = choose automatically, the default).  A larger
+ * cap raises parallelism for few long sequences; the merge costs a little
+ * extra memory traffic.  Process-wide.
+ */
+pkv_status pkv_set_max_splits(int32_t max_splits);
+
+/*
+ * Allocate, on the current device, the decode workspace for batches up to
+ * the given shape, so that later calls of that size or smaller never
+ * allocate (required before stream capture).  Grows, never shrinks.
+ */
+pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_blocks_per_seq);
+
+/*
+ * Bound, in nanoseconds, on every wait inside the kernels (default
+ * 1000000000).  When a wait expires the kernel records PKV_ERR_TIMEOUT,
+ * lets its own copies in flight land, releases its tensor memory and
+ * returns; the context stays usable.  0 makes the first wait of every block
+ * expire at once, which tests that path.  Process-wide.
+ */
+pkv_status pkv_set_wait_limit_ns(int64_t limit_ns);
+
+/*
+ * Kernel timing: while enabled, every kernel launch of the library is
+ * bracketed by CUDA events on its own stream.  pkv_profiler_read
+ * synchronises the recorded events and returns, for kernel `name`
+ * ("store_kvcache", "decode_split", "decode_combine", "prefill"), the summed
+ * duration in milliseconds and the launch count since the last reset.
+ */
+pkv_status pkv_profiler_enable(int32_t enable);
+pkv_status pkv_profiler_reset(void);
+pkv_status pkv_profiler_read(const char* name, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,479 @@
+// pkv_api.cu -- the extern "C" entry points of libpkv (declared in pkv.h):
+// host-side validation, per-device state (error word, decode workspace,
+// tensor-map cache), the split-K plan, and the kernel-timing profiler.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+using pkv::CacheMaps;
+using pkv::DeviceError;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMapCacheSize = 8;
+
+struct MapEntry {
+  const void* k = nullptr;
+  const void* v = nullptr;
+  int64_t num_blocks = 0;
+  int hkv = 0, d = 0;
+  uint64_t stamp = 0;
+  CacheMaps maps;
+};
+
+struct DeviceState {
+  bool ready = false;
+  bool usable = false;
+  int num_sms = 0;
+  DeviceError* err = nullptr;
+  float* ws = nullptr;
+  size_t ws_bytes = 0;
+  MapEntry maps[kMapCacheSize];
+  uint64_t clock = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+pkv::EncodeTiledFn g_encode = nullptr;
+std::atomic<int> g_max_splits{0};
+std::atomic<int64_t> g_wait_limit_ns{1000000000};
+
+// ------------------------------------------------------------------ profiler
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+std::atomic<int> g_prof_on{0};
+std::vector<ProfRecord> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+template <typename F>
+cudaError_t timed_launch(const char* name, cudaStream_t stream, F&& launch) {
+  if (!g_prof_on.load()) return launch();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t a = take_event(), b = take_event();
+  if (!a || !b) return cudaErrorMemoryAllocation;
+  cudaEventRecord(a, stream);
+  cudaError_t e = launch();
+  cudaEventRecord(b, stream);
+  g_prof.push_back({name, a, b});
+  return e;
+}
+
+// ------------------------------------------------------------------ helpers
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  if (e == cudaErrorMemoryAllocation) return PKV_ERR_NO_MEMORY;
+  return PKV_ERR_CUDA;
+}
+
+bool load_encoder() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<pkv::EncodeTiledFn>(fn);
+  return true;
+}
+
+// Must be called with g_mu held.
+DeviceState* device_state(pkv_status* st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *st = PKV_ERR_CUDA;
+    return nullptr;
+  }
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    d.usable = (major == 10 && minor == 3) && load_encoder();
+    if (d.usable) {
+      if (cudaMalloc(&d.err, sizeof(DeviceError)) != cudaSuccess ||
+          cudaMemset(d.err, 0, sizeof(DeviceError)) != cudaSuccess) {
+        d.usable = false;
+      }
+    }
+    cudaGetLastError();
+  }
+  if (!d.usable) {
+    *st = PKV_ERR_CUDA;
+    return nullptr;
+  }
+  *st = PKV_OK;
+  return &d;
+}
+
+bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
+               uint32_t b2, CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps over the cache viewed as [slots][Hkv][D] (3-D: D, Hkv, slots).
+const CacheMaps* cache_maps(DeviceState* ds, const void* k, const void* v, int64_t num_blocks,
+                            int hkv, int d) {
+  ++ds->clock;
+  for (auto& e : ds->maps) {
+    if (e.k == k && e.v == v && e.num_blocks == num_blocks && e.hkv == hkv && e.d == d) {
+      e.stamp = ds->clock;
+      return &e.maps;
+    }
+  }
+  MapEntry* victim = &ds->maps[0];
+  for (auto& e : ds->maps)
+    if (e.stamp < victim->stamp) victim = &e;
+  const uint64_t slots = static_cast<uint64_t>(num_blocks) * pkv::kBlockSize;
+  const uint64_t s1 = static_cast<uint64_t>(d) * 2;
+  const uint64_t s2 = static_cast<uint64_t>(hkv) * d * 2;
+  MapEntry e;
+  bool ok = encode_3d(&e.maps.k_rows, k, d, hkv, slots, s1, s2, d, 1, pkv::kDecodeChunk,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_3d(&e.maps.v_rows, v, d, hkv, slots, s1, s2, d, 1, pkv::kDecodeChunk,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
+            encode_3d(&e.maps.k_sw128, k, d, hkv, slots, s1, s2, 64, 1, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_3d(&e.maps.v_sw128, v, d, hkv, slots, s1, s2, 64, 1, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return nullptr;
+  e.k = k;
+  e.v = v;
+  e.num_blocks = num_blocks;
+  e.hkv = hkv;
+  e.d = d;
+  e.stamp = ds->clock;
+  *victim = e;
+  return &victim->maps;
+}
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+// Split-K plan: enough (sequence, KV head, split) blocks to fill the GPU
+// several times over, splits a multiple of 64 tokens.
+void plan_splits(int num_seqs, int hkv, int max_blocks, int num_sms, int* split_tokens,
+                 int* max_splits) {
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * pkv::kBlockSize;
+  const int64_t units = static_cast<int64_t>(num_seqs) * hkv;
+  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 16;
+  int64_t want = (target + units - 1) / units;
+  if (want < 1) want = 1;
+  int64_t split = (max_ctx + want - 1) / want;
+  split = ((split + 63) / 64) * 64;
+  const int cap = g_max_splits.load();
+  if (cap > 0) {
+    int64_t min_split = (max_ctx + cap - 1) / cap;
+    min_split = ((min_split + 63) / 64) * 64;
+    if (split < min_split) split = min_split;
+  }
+  if (split < 64) split = 64;
+  *split_tokens = static_cast<int>(split);
+  *max_splits = static_cast<int>((max_ctx + split - 1) / split);
+}
+
+pkv_status ensure_workspace(DeviceState* ds, size_t bytes) {
+  if (bytes <= ds->ws_bytes) return PKV_OK;
+  if (ds->ws) cudaFree(ds->ws);
+  ds->ws = nullptr;
+  ds->ws_bytes = 0;
+  if (cudaMalloc(&ds->ws, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_NO_MEMORY;
+  }
+  ds->ws_bytes = bytes;
+  return PKV_OK;
+}
+
+size_t decode_ws_bytes(int num_seqs, int hq, int d, int max_splits) {
+  const size_t rows = static_cast<size_t>(num_seqs) * hq * max_splits;
+  return rows * d * sizeof(float) + rows * 2 * sizeof(float) + 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    case PKV_ERR_NO_MEMORY: return "PKV_ERR_NO_MEMORY";
+  }
+  return "PKV_ERR_UNKNOWN";
+}
+
+const char* pkv_version(void) { return "pkv 0.1.0 sm_103a"; }
+
+pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
+                             int64_t v_row_stride, const int32_t* slot_mapping,
+                             int64_t num_tokens, void* k_cache, void* v_cache,
+                             int64_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                             pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return PKV_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_row_stride < row || v_row_stride < row) return PKV_ERR_INVALID_ARG;
+  if ((row * 2) % 16 || (k_row_stride * 2) % 16 || (v_row_stride * 2) % 16)
+    return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > (int64_t{1} << 31) / pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  pkv_status st;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ds = device_state(&st);
+  }
+  if (!ds) return st;
+  if (num_tokens == 0) return PKV_OK;
+  pkv::StoreArgs a{k, v, k_row_stride, v_row_stride, slot_mapping, num_tokens, k_cache, v_cache,
+                   num_blocks, num_kv_heads, head_dim, ds->err};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(
+      timed_launch("store_kvcache", s, [&] { return pkv::launch_store_kvcache(a, s); }));
+}
+
+static pkv_status validate_attention(const void* q, int64_t q_row_stride, const void* k_cache,
+                                     const void* v_cache, int64_t num_blocks,
+                                     const int32_t* block_tables, int32_t max_blocks,
+                                     const int32_t* lens, int32_t num_seqs, int32_t hq,
+                                     int32_t hkv, int32_t d, const void* out) {
+  if (num_seqs < 0 || num_blocks <= 0 || max_blocks <= 0 || hq <= 0 || hkv <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || !q || !block_tables || !lens || !out) return PKV_ERR_INVALID_ARG;
+  if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PKV_ERR_UNSUPPORTED;
+  if (!supported_group(hq / hkv)) return PKV_ERR_UNSUPPORTED;
+  if (q_row_stride < static_cast<int64_t>(hq) * d) return PKV_ERR_INVALID_ARG;
+  if ((q_row_stride * 2) % 16) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > (int64_t{1} << 31) / pkv::kBlockSize ||
+      max_blocks > (int64_t{1} << 31) / pkv::kBlockSize)
+    return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
+                                const void* v_cache, int64_t num_blocks,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t num_seqs,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                float scale, void* out, pkv_stream_t stream) {
+  pkv_status st = validate_attention(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                                     num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  pkv::DecodeArgs a{};
+  const CacheMaps* maps = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0) return PKV_OK;
+    maps = cache_maps(ds, k_cache, v_cache, num_blocks, num_kv_heads, head_dim);
+    if (!maps) return PKV_ERR_CUDA;
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
+    a.err = ds->err;
+    plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, ds->num_sms, &a.split_tokens,
+                &a.max_splits);
+    if (a.max_splits > 1) {
+      st = ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, a.max_splits));
+      if (st != PKV_OK) return st;
+      a.part_o = ds->ws;
+      a.part_ml = ds->ws + static_cast<size_t>(num_seqs) * num_q_heads * a.max_splits * head_dim;
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CacheMaps m = *maps;
+  cudaError_t e = timed_launch("decode_split", s, [&] { return pkv::launch_decode_split(a, m, s); });
+  if (e == cudaSuccess)
+    e = timed_launch("decode_combine", s, [&] { return pkv::launch_decode_combine(a, s); });
+  return cuda_status(e);
+}
+
+pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void* k_cache,
+                                 const void* v_cache, int64_t num_blocks,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                 int32_t num_seqs, int64_t total_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
+                                 pkv_stream_t stream) {
+  pkv_status st = validate_attention(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                                     num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  if (!cu_seqlens_q || total_q < 0 || total_q > 0x7FFFFFFF) return PKV_ERR_INVALID_ARG;
+  pkv::PrefillArgs a{};
+  CacheMaps m;
+  CUtensorMap qmap;
+  int num_sms = 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    const CacheMaps* maps = cache_maps(ds, k_cache, v_cache, num_blocks, num_kv_heads, head_dim);
+    if (!maps) return PKV_ERR_CUDA;
+    m = *maps;
+    const int g = num_q_heads / num_kv_heads;
+    if (!encode_3d(&qmap, q, head_dim, num_q_heads, total_q, static_cast<uint64_t>(head_dim) * 2,
+                   static_cast<uint64_t>(q_row_stride) * 2, 64, g, 128 / g,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    num_sms = ds->num_sms;
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
+    a.err = ds->err;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(
+      timed_launch("prefill", s, [&] { return pkv::launch_prefill(a, m, qmap, num_sms, s); }));
+}
+
+pkv_status pkv_get_device_error(pkv_stream_t stream, int32_t* code, int32_t* info) {
+  if (!code) return PKV_ERR_INVALID_ARG;
+  pkv_status st;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ds = device_state(&st);
+  }
+  if (!ds) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+  DeviceError h{0, 0};
+  if (cudaMemcpy(&h, ds->err, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemset(ds->err, 0, sizeof h) != cudaSuccess) return PKV_ERR_CUDA;
+  *code = h.code;
+  if (info) *info = h.info;
+  return PKV_OK;
+}
+
+pkv_status pkv_set_max_splits(int32_t max_splits) {
+  if (max_splits < 0) return PKV_ERR_INVALID_ARG;
+  g_max_splits.store(max_splits);
+  return PKV_OK;
+}
+
+pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_blocks_per_seq) {
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 ||
+      (head_dim != 64 && head_dim != 128))
+    return PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  pkv_status st;
+  DeviceState* ds = device_state(&st);
+  if (!ds) return st;
+  // The plan never uses more splits than one per 64 tokens of the longest context.
+  const int max_splits = (max_blocks_per_seq * pkv::kBlockSize + 63) / 64;
+  int split_tokens = 0, splits = 0;
+  plan_splits(num_seqs, 1, max_blocks_per_seq, ds->num_sms, &split_tokens, &splits);
+  (void)max_splits;
+  return ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, splits));
+}
+
+pkv_status pkv_set_wait_limit_ns(int64_t limit_ns) {
+  if (limit_ns < 0) return PKV_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(limit_ns);
+  return PKV_OK;
+}
+
+pkv_status pkv_profiler_enable(int32_t enable) {
+  g_prof_on.store(enable ? 1 : 0);
+  return PKV_OK;
+}
+
+pkv_status pkv_profiler_reset(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_prof.clear();
+  return PKV_OK;
+}
+
+pkv_status pkv_profiler_read(const char* name, double* total_ms, int64_t* launches) {
+  if (!name || !total_ms || !launches) return PKV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  double sum = 0.0;
+  int64_t n = 0;
+  for (auto& r : g_prof) {
+    if (std::strcmp(r.name, name) != 0) continue;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return PKV_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return PKV_ERR_CUDA;
+    sum += ms;
+    ++n;
+  }
+  *total_ms = sum;
+  *launches = n;
+  return PKV_OK;
+}
+
+}  // extern "C"
