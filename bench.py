@@ -371,11 +371,13 @@ def run_gpu(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def other_workloads(pkv, args, rank, flush, peaks):
+def other_workloads(pkv, args, rank, flush, peaks, only=None):
     res = {}
     steps = max(3, min(args.steps, 10))
     # Long-context and prefix-sharing decode.
     for name, make in (("long_decode_32k", W.long_decode), ("prefix_decode_b64", W.prefix_decode)):
+        if only is not None and name != only:
+            continue
         case = make(seed=replica_seed(1003 if name.startswith("long") else 1004, rank))
         b = decode_step_bytes(case)
         bench = DecodeBench(case, pkv)
@@ -397,6 +399,8 @@ def other_workloads(pkv, args, rank, flush, peaks):
         res[name] = entry
         del bench
         torch.cuda.empty_cache()
+    if only is not None and only != "chunked_prefill_8x512":
+        return res
     # Chunked prefill.
     case = W.chunked_prefill(seed=replica_seed(1005, rank))
     c = case.cache
@@ -424,6 +428,19 @@ def other_workloads(pkv, args, rank, flush, peaks):
         "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
         "store_ms": round(st_ms, 5), "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
     return res
+
+
+def run_single(args, rank, world, local):
+    """One non-default workload alone: its warm-up and timed steps, one JSON line."""
+    import paged_kv_cache_493_b300 as pkv
+    from paged_kv_cache_493_b300 import _build
+    _build.build()
+    pkv.load_library()
+    torch.cuda.set_device(local)
+    peaks, _ = load_peaks()
+    res = other_workloads(pkv, args, rank, Flusher(), peaks, only=args.workload)
+    if rank == 0:
+        print(json.dumps({"workload": args.workload, **res[args.workload]}), flush=True)
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -497,6 +514,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
+    ap.add_argument("--workload", default=MAIN_WORKLOAD,
+                    choices=[MAIN_WORKLOAD, "long_decode_32k", "prefix_decode_b64",
+                             "chunked_prefill_8x512"],
+                    help="run one non-default workload alone (for profiling) and print its entry")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "pkv":
         args.warmup = 3
@@ -504,6 +525,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.workload != MAIN_WORKLOAD:
+            run_single(args, rank, world, local)
         else:
             run_gpu(args, rank, world, local)
     finally:
