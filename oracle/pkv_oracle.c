@@ -157,6 +157,17 @@ void oracle_attend(const double* q, const double* K, const double* V, int32_t nu
   free(x);
 }
 
+/* A (row, head) pair listed more than once in a sampled request receives
+ * the same output at every position it is listed. */
+static void copy_to_repeats(const int32_t* rows, int32_t n_rows, int32_t first, int32_t r,
+                            int32_t h, double* out, int32_t head_dim) {
+  if (!rows || first < 0) return;
+  for (int32_t i = first + 1; i < n_rows; ++i)
+    if (rows[2 * i] == r && rows[2 * i + 1] == h)
+      memcpy(out + (int64_t)i * head_dim, out + (int64_t)first * head_dim,
+             sizeof(double) * (size_t)head_dim);
+}
+
 static int check_heads(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim) {
   if (num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORACLE_BAD_ARG;
   if (num_q_heads % num_kv_heads != 0) return ORACLE_BAD_ARG;
@@ -203,15 +214,18 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
                        block_tables + (int64_t)s * max_blocks, max_blocks, ctx, K, V);
     for (int32_t h = 0; h < num_q_heads && rc == ORACLE_OK; ++h) {
       double* dst = NULL;
+      int32_t first = -1;
       if (rows == NULL) {
         dst = out + ((int64_t)s * num_q_heads + h) * head_dim;
       } else {
-        for (int32_t i = 0; i < n_rows; ++i)
-          if (rows[2 * i] == s && rows[2 * i + 1] == h) dst = out + (int64_t)i * head_dim;
+        for (int32_t i = 0; i < n_rows && first < 0; ++i)
+          if (rows[2 * i] == s && rows[2 * i + 1] == h) first = i;
+        if (first >= 0) dst = out + (int64_t)first * head_dim;
       }
       if (!dst) continue;
       oracle_bf16_to_f64(q + ((int64_t)s * num_q_heads + h) * head_dim, head_dim, qrow);
       oracle_attend(qrow, K, V, num_kv_heads, head_dim, h / group, ctx, scale, dst, NULL);
+      copy_to_repeats(rows, n_rows, first, s, h, out, head_dim);
     }
     free(K);
     free(V);
@@ -270,15 +284,18 @@ int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v
       const int32_t n_keys = ctx - lq + (tok - t0) + 1;
       for (int32_t h = 0; h < num_q_heads; ++h) {
         double* dst = NULL;
+        int32_t first = -1;
         if (rows == NULL) {
           dst = out + ((int64_t)tok * num_q_heads + h) * head_dim;
         } else {
-          for (int32_t i = 0; i < n_rows; ++i)
-            if (rows[2 * i] == tok && rows[2 * i + 1] == h) dst = out + (int64_t)i * head_dim;
+          for (int32_t i = 0; i < n_rows && first < 0; ++i)
+            if (rows[2 * i] == tok && rows[2 * i + 1] == h) first = i;
+          if (first >= 0) dst = out + (int64_t)first * head_dim;
         }
         if (!dst) continue;
         oracle_bf16_to_f64(q + ((int64_t)tok * num_q_heads + h) * head_dim, head_dim, qrow);
         oracle_attend(qrow, K, V, num_kv_heads, head_dim, h / group, n_keys, scale, dst, NULL);
+        copy_to_repeats(rows, n_rows, first, tok, h, out, head_dim);
       }
     }
     free(K);

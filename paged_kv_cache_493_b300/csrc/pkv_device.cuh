@@ -83,11 +83,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// limit_ns nanoseconds.  limit_ns == 0 fails at once unless the phase has
-// already completed.  Returns false on expiry.
+// limit_ns nanoseconds.  Returns false on expiry.  limit_ns == 0 fails at
+// once without looking at the barrier (try_wait itself may suspend until the
+// phase completes, so a zero budget could otherwise still succeed); this is
+// the hook that exercises the abort path.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
   if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t start = global_timer_ns();
   while (true) {
 #pragma unroll 1

@@ -352,7 +352,7 @@ def test_sampled_rows_equal_full_output():
     c = case.cache
     full = oracle.prefill(case.q, c.k_cache, c.v_cache, c.block_tables, case.cu_seqlens_q,
                           c.context_lens, case.scale)
-    rows = [(0, 0), (19, 3), (20, 1), (26, 2)]
+    rows = [(0, 0), (19, 3), (20, 1), (26, 2), (0, 0), (19, 3)]   # repeats allowed
     part = oracle.prefill(case.q, c.k_cache, c.v_cache, c.block_tables, case.cu_seqlens_q,
                           c.context_lens, case.scale, rows=rows)
     for i, (t, h) in enumerate(rows):
@@ -360,7 +360,7 @@ def test_sampled_rows_equal_full_output():
     dcase = W.tiny_decode()
     dc = dcase.cache
     dfull = oracle.decode(dcase.q, dc.k_cache, dc.v_cache, dc.block_tables, dc.context_lens, dcase.scale)
-    drows = [(3, 1), (0, 2)]
+    drows = [(3, 1), (0, 2), (3, 1)]
     dpart = oracle.decode(dcase.q, dc.k_cache, dc.v_cache, dc.block_tables, dc.context_lens,
                           dcase.scale, rows=drows)
     for i, (s, h) in enumerate(drows):
