@@ -171,12 +171,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         tma_load_3d(smem_u32(&sm.v[st][0][0]), &vmap, fb, 0, kvh, slot);
         last_issued[st] = c;
       }
-      // Copies still in flight must land before the block may exit.
-      if (*reinterpret_cast<volatile int*>(&sm.abort_flag)) {
-        for (int s = 0; s < kStages; ++s)
-          if (last_issued[s] >= 0)
-            mbar_wait(smem_u32(&sm.full[s]), (last_issued[s] / kStages) & 1, kDrainLimitNs);
-      }
+      // Every copy issued must land before the block may exit, whether or
+      // not the consumers gave up on it (after a normal run these waits
+      // return at once: the consumers have already seen each phase).
+      for (int s = 0; s < kStages; ++s)
+        if (last_issued[s] >= 0)
+          mbar_wait(smem_u32(&sm.full[s]), (last_issued[s] / kStages) & 1, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------------ consumers

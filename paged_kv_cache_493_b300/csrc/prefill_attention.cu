@@ -232,12 +232,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                       bar.v_full[st], p * 64, kvh, slot);
         v_last[st] = j;
       }
-      if (misc[1]) {  // let every copy already issued land before exiting
-        mbar_wait(bar.q_full, 0, kDrainLimitNs);
-        for (int s = 0; s < 2; ++s) {
-          if (k_last[s] >= 0) mbar_wait(bar.k_full[s], (k_last[s] >> 1) & 1, kDrainLimitNs);
-          if (v_last[s] >= 0) mbar_wait(bar.v_full[s], (v_last[s] >> 1) & 1, kDrainLimitNs);
-        }
+      // Every copy issued must land before the block may exit, whether or
+      // not its consumer gave up on it (after a normal run these waits
+      // return at once).
+      mbar_wait(bar.q_full, 0, kDrainLimitNs);
+      for (int s = 0; s < 2; ++s) {
+        if (k_last[s] >= 0) mbar_wait(bar.k_full[s], (k_last[s] >> 1) & 1, kDrainLimitNs);
+        if (v_last[s] >= 0) mbar_wait(bar.v_full[s], (v_last[s] >> 1) & 1, kDrainLimitNs);
       }
     }
   } else if (warp == 5) {
@@ -300,11 +301,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           tc_commit(bar.v_empty[st]);
         }
       }
-      if (!ok) {
-        misc[1] = 1;
-        tc_commit(bar.drain);  // every MMA issued so far must finish before exit
-        mbar_wait(bar.drain, 0, kDrainLimitNs);
-      }
+      if (!ok) misc[1] = 1;
+      // Every MMA issued must finish before tensor memory is released.
+      tc_commit(bar.drain);
+      mbar_wait(bar.drain, 0, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
