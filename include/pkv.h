@@ -155,6 +155,48 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
                                  int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
                                  pkv_stream_t stream);
 
+/*
+ * pkv_decode_attention_noalloc -- pkv_decode_attention for callers that
+ * cannot let the library allocate device memory: serving engines that hand
+ * nearly all free memory to the KV block pool at start-up, code running
+ * while a stream is captured into a CUDA graph (where cudaMalloc is not
+ * allowed), and processes whose device memory must all come from one
+ * caching allocator.  The pages describe no such variant; it is an
+ * addition of this library.
+ *
+ * Arguments, layouts, results and the split plan are those of
+ * pkv_decode_attention.  The difference is where the split-K partials go:
+ * into a 16 MiB array that the library defines statically on every device
+ * that loads it (held until the process exits), not into a cudaMalloc'ed
+ * workspace.  The call itself calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ * - Size limit: num_seqs * num_q_heads * splits * (head_dim + 2) * 4 bytes
+ *   must fit in 16 MiB - 256 bytes, where splits is the plan's number of
+ *   context ranges for a context of 256 * max_blocks_per_seq tokens (about
+ *   148 * 16 / (num_seqs * num_kv_heads) ranges, capped by
+ *   pkv_set_max_splits).  A batch that needs more returns
+ *   PKV_ERR_UNSUPPORTED and launches nothing.  A plan of one range uses no
+ *   scratch at all.
+ * - Set-up: the first call on each device, with that device current, looks
+ *   up the array's device address (cudaGetSymbolAddress); make that first
+ *   call before any stream capture.
+ * - Sharing: every call on a device uses the same array, which keeps the
+ *   last call's contents (the kernels write every partial they read, so
+ *   nothing needs clearing).  Calls whose kernels overlap on the GPU (on
+ *   different streams without ordering) race on it: serialise them.
+ * - Device-side checks still zero the output rows of out-of-range block ids
+ *   or lengths, but their error code goes to a word inside the array and is
+ *   not reported by pkv_get_device_error.
+ */
+pkv_status pkv_decode_attention_noalloc(const void* q, int64_t q_row_stride, const void* k_cache,
+                                        const void* v_cache, int64_t num_blocks,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, float scale, void* out,
+                                        pkv_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Helpers
  * --------------------------------------------------------------------- */

@@ -36,6 +36,8 @@ SIGNATURES = {
                               _P, _P], _I32),
     "pkv_prefill_attention": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _P, _I32, _I64, _I32, _I32,
                                _I32, _F, _P, _P], _I32),
+    "pkv_decode_attention_noalloc": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
+                                      _I32, _F, _P, _P], _I32),
     "pkv_status_string": ([_I32], ctypes.c_char_p),
     "pkv_version": ([], ctypes.c_char_p),
     "pkv_get_device_error": ([_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)], _I32),
@@ -151,6 +153,29 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
         _ptr(context_lens), b, hq, hkv, d, float(scale), _ptr(out), _stream(stream)),
         "pkv_decode_attention")
+
+
+def pkv_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                 out, stream=None) -> None:
+    """pkv_decode_attention with its split-K scratch in the library's static
+    16 MiB device array: the call allocates no device memory, for callers that
+    cannot allocate (a KV pool that already holds the free memory, stream
+    capture).  Raises PkvError(PKV_ERR_UNSUPPORTED) for a batch whose partials
+    do not fit; overlapping calls on one device race on the shared array."""
+    nb, hkv, d = _cache(k_cache, v_cache)
+    _need(q.dim() == 3, "q: [B, Hq, D]")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    qs = _rows(q, "q", hq, d)
+    _i32(block_tables, "block_tables")
+    _i32(context_lens, "context_lens")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == b, "block_tables: [B, max_blocks]")
+    _need(context_lens.numel() == b, "context_lens: [B]")
+    _need(out.is_contiguous() and out.shape == q.shape and out.dtype == q.dtype and out.is_cuda,
+          "out: contiguous, same shape/dtype as q")
+    _check(load_library().pkv_decode_attention_noalloc(
+        _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(context_lens), b, hq, hkv, d, float(scale), _ptr(out), _stream(stream)),
+        "pkv_decode_attention_noalloc")
 
 
 def pkv_prefill_attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, context_lens,

@@ -1,0 +1,137 @@
+// decode_noalloc.cu -- pkv_decode_attention_noalloc: the paged decode call
+// with its split-K scratch in a fixed device array that the library defines
+// at file scope, so that the call itself allocates nothing.
+//
+// Who needs it: callers that cannot let a library call cudaMalloc.
+//  - Serving engines that give (nearly) all free device memory to the KV
+//    block pool at start-up: a workspace allocated later by the library can
+//    fail for lack of memory, or sit outside the engine's own accounting.
+//  - Code that runs while a stream is captured into a CUDA graph, where a
+//    cudaMalloc is not allowed.
+//  - Processes whose device memory must all go through one caching
+//    allocator.
+// pkv_decode_attention grows a cudaMalloc'ed workspace on first need; this
+// entry point uses the static array below instead, and the caller still
+// passes every input and output.
+//
+// The array is part of the library image: every device that loads libpkv
+// holds its kScratchBytes until the process exits.  Host code cannot use the
+// array's name as a device address (on the host it names a stand-in), so
+// the first call on each device, with that device current, asks the runtime
+// for the device address with cudaGetSymbolAddress and keeps it.  That
+// first call should therefore come before any stream capture.
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace {
+
+// Size of the per-device scratch: the split-K partials of one call,
+// num_seqs * num_q_heads * splits * (head_dim + 2) fp32 values, after a
+// 256-byte word for the kernels' device-side error reports.
+constexpr size_t kScratchBytes = size_t{16} << 20;
+constexpr size_t kErrBytes = 256;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+
+struct NoAllocDevice {
+  bool ready = false;
+  bool usable = false;
+  int num_sms = 0;
+  unsigned char* scratch = nullptr;  // device address of g_decode_scratch
+};
+
+std::mutex g_mu;
+NoAllocDevice g_dev[kMaxDevices];
+
+// Once per device, with that device current: check the architecture, find
+// the tensor-map encoder and look up the device address of the scratch.
+// Must be called with g_mu held.
+NoAllocDevice* device_setup(pkv_status* st) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *st = PKV_ERR_CUDA;
+    return nullptr;
+  }
+  NoAllocDevice& d = g_dev[dev];
+  if (!d.ready) {
+    d.ready = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    void* ptr = nullptr;
+    d.usable = major == 10 && minor == 3 && pkv::load_tensor_map_encoder() &&
+               cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess && ptr != nullptr;
+    d.scratch = static_cast<unsigned char*>(ptr);
+    cudaGetLastError();
+  }
+  if (!d.usable) {
+    *st = PKV_ERR_CUDA;
+    return nullptr;
+  }
+  *st = PKV_OK;
+  return &d;
+}
+
+}  // namespace
+
+extern "C" pkv_status pkv_decode_attention_noalloc(
+    const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+    int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, float scale, void* out, pkv_stream_t stream) {
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_cache, v_cache, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  int num_sms = 0;
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocDevice* d = device_setup(&st);
+    if (!d) return st;
+    num_sms = d->num_sms;
+    scratch = d->scratch;
+  }
+  if (num_seqs == 0) return PKV_OK;
+
+  pkv::DecodeArgs a{};
+  a.q = q;
+  a.q_row_stride = q_row_stride;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.out = out;
+  a.wait_limit_ns = pkv::wait_limit_ns();
+  a.err = reinterpret_cast<pkv::DeviceError*>(scratch);
+  pkv::plan_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, num_sms, &a.split_tokens,
+                          &a.max_splits);
+  if (a.max_splits > 1) {
+    // Partials of every (sequence, query head, range): head_dim + 2 fp32.
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * a.max_splits;
+    const size_t need = rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+    if (need > kScratchBytes - kErrBytes) return PKV_ERR_UNSUPPORTED;
+    a.part_o = reinterpret_cast<float*>(scratch + kErrBytes);
+    a.part_ml = a.part_o + rows * head_dim;
+  }
+
+  pkv::CacheMaps maps;
+  if (!pkv::encode_cache_maps(&maps, k_cache, v_cache, num_blocks, num_kv_heads, head_dim))
+    return PKV_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = pkv::launch_decode_split(a, maps, s);
+  if (e == cudaSuccess) e = pkv::launch_decode_combine(a, s);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -158,19 +158,8 @@ const CacheMaps* cache_maps(DeviceState* ds, const void* k, const void* v, int64
   MapEntry* victim = &ds->maps[0];
   for (auto& e : ds->maps)
     if (e.stamp < victim->stamp) victim = &e;
-  const uint64_t slots = static_cast<uint64_t>(num_blocks) * pkv::kBlockSize;
-  const uint64_t s1 = static_cast<uint64_t>(d) * 2;
-  const uint64_t s2 = static_cast<uint64_t>(hkv) * d * 2;
   MapEntry e;
-  bool ok = encode_3d(&e.maps.k_rows, k, d, hkv, slots, s1, s2, d, 1, pkv::kDecodeChunk,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_3d(&e.maps.v_rows, v, d, hkv, slots, s1, s2, d, 1, pkv::kDecodeChunk,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) &&
-            encode_3d(&e.maps.k_sw128, k, d, hkv, slots, s1, s2, 64, 1, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B) &&
-            encode_3d(&e.maps.v_sw128, v, d, hkv, slots, s1, s2, 64, 1, 128,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  if (!ok) return nullptr;
+  if (!pkv::encode_cache_maps(&e.maps, k, v, num_blocks, hkv, d)) return nullptr;
   e.k = k;
   e.v = v;
   e.num_blocks = num_blocks;
@@ -182,28 +171,6 @@ const CacheMaps* cache_maps(DeviceState* ds, const void* k, const void* v, int64
 }
 
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
-
-// Split-K plan: enough (sequence, KV head, split) blocks to fill the GPU
-// several times over, splits a multiple of 64 tokens.
-void plan_splits(int num_seqs, int hkv, int max_blocks, int num_sms, int* split_tokens,
-                 int* max_splits) {
-  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * pkv::kBlockSize;
-  const int64_t units = static_cast<int64_t>(num_seqs) * hkv;
-  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 16;
-  int64_t want = (target + units - 1) / units;
-  if (want < 1) want = 1;
-  int64_t split = (max_ctx + want - 1) / want;
-  split = ((split + 63) / 64) * 64;
-  const int cap = g_max_splits.load();
-  if (cap > 0) {
-    int64_t min_split = (max_ctx + cap - 1) / cap;
-    min_split = ((min_split + 63) / 64) * 64;
-    if (split < min_split) split = min_split;
-  }
-  if (split < 64) split = 64;
-  *split_tokens = static_cast<int>(split);
-  *max_splits = static_cast<int>((max_ctx + split - 1) / split);
-}
 
 pkv_status ensure_workspace(DeviceState* ds, size_t bytes) {
   if (bytes <= ds->ws_bytes) return PKV_OK;
@@ -224,6 +191,73 @@ size_t decode_ws_bytes(int num_seqs, int hq, int d, int max_splits) {
 }
 
 }  // namespace
+
+namespace pkv {
+
+// Split-K plan: enough (sequence, KV head, split) blocks to fill the GPU
+// several times over, splits a multiple of 64 tokens.
+void plan_decode_splits(int num_seqs, int hkv, int max_blocks, int num_sms, int* split_tokens,
+                        int* max_splits) {
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * kBlockSize;
+  const int64_t units = static_cast<int64_t>(num_seqs) * hkv;
+  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 16;
+  int64_t want = (target + units - 1) / units;
+  if (want < 1) want = 1;
+  int64_t split = (max_ctx + want - 1) / want;
+  split = ((split + 63) / 64) * 64;
+  const int cap = g_max_splits.load();
+  if (cap > 0) {
+    int64_t min_split = (max_ctx + cap - 1) / cap;
+    min_split = ((min_split + 63) / 64) * 64;
+    if (split < min_split) split = min_split;
+  }
+  if (split < 64) split = 64;
+  *split_tokens = static_cast<int>(split);
+  *max_splits = static_cast<int>((max_ctx + split - 1) / split);
+}
+
+// Tensor maps over the cache viewed as [slots][Hkv][D] (3-D: D, Hkv, slots).
+bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t num_blocks, int hkv,
+                       int d) {
+  const uint64_t slots = static_cast<uint64_t>(num_blocks) * kBlockSize;
+  const uint64_t s1 = static_cast<uint64_t>(d) * 2;
+  const uint64_t s2 = static_cast<uint64_t>(hkv) * d * 2;
+  return encode_3d(&maps->k_rows, k, d, hkv, slots, s1, s2, d, 1, kDecodeChunk,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_3d(&maps->v_rows, v, d, hkv, slots, s1, s2, d, 1, kDecodeChunk,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_3d(&maps->k_sw128, k, d, hkv, slots, s1, s2, 64, 1, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_3d(&maps->v_sw128, v, d, hkv, slots, s1, s2, 64, 1, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool load_tensor_map_encoder() { return load_encoder(); }
+
+uint64_t wait_limit_ns() { return static_cast<uint64_t>(g_wait_limit_ns.load()); }
+
+pkv_status validate_attention_args(const void* q, int64_t q_row_stride, const void* k_cache,
+                                   const void* v_cache, int64_t num_blocks,
+                                   const int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* lens, int32_t num_seqs, int32_t hq, int32_t hkv,
+                                   int32_t d, const void* out) {
+  if (num_seqs < 0 || num_blocks <= 0 || max_blocks <= 0 || hq <= 0 || hkv <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!k_cache || !v_cache || !q || !block_tables || !lens || !out) return PKV_ERR_INVALID_ARG;
+  if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PKV_ERR_UNSUPPORTED;
+  if (!supported_group(hq / hkv)) return PKV_ERR_UNSUPPORTED;
+  if (q_row_stride < static_cast<int64_t>(hq) * d) return PKV_ERR_INVALID_ARG;
+  if ((q_row_stride * 2) % 16) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > (int64_t{1} << 31) / pkv::kBlockSize ||
+      max_blocks > (int64_t{1} << 31) / pkv::kBlockSize)
+    return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace pkv
 
 extern "C" {
 
@@ -273,36 +307,15 @@ pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
       timed_launch("store_kvcache", s, [&] { return pkv::launch_store_kvcache(a, s); }));
 }
 
-static pkv_status validate_attention(const void* q, int64_t q_row_stride, const void* k_cache,
-                                     const void* v_cache, int64_t num_blocks,
-                                     const int32_t* block_tables, int32_t max_blocks,
-                                     const int32_t* lens, int32_t num_seqs, int32_t hq,
-                                     int32_t hkv, int32_t d, const void* out) {
-  if (num_seqs < 0 || num_blocks <= 0 || max_blocks <= 0 || hq <= 0 || hkv <= 0)
-    return PKV_ERR_INVALID_ARG;
-  if (!k_cache || !v_cache || !q || !block_tables || !lens || !out) return PKV_ERR_INVALID_ARG;
-  if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return PKV_ERR_UNSUPPORTED;
-  if (!supported_group(hq / hkv)) return PKV_ERR_UNSUPPORTED;
-  if (q_row_stride < static_cast<int64_t>(hq) * d) return PKV_ERR_INVALID_ARG;
-  if ((q_row_stride * 2) % 16) return PKV_ERR_UNSUPPORTED;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return PKV_ERR_UNSUPPORTED;
-  if (num_blocks > (int64_t{1} << 31) / pkv::kBlockSize ||
-      max_blocks > (int64_t{1} << 31) / pkv::kBlockSize)
-    return PKV_ERR_UNSUPPORTED;
-  return PKV_OK;
-}
-
 pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
                                 const void* v_cache, int64_t num_blocks,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 const int32_t* context_lens, int32_t num_seqs,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                 float scale, void* out, pkv_stream_t stream) {
-  pkv_status st = validate_attention(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
-                                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
-                                     num_kv_heads, head_dim, out);
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_cache, v_cache, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
   if (st != PKV_OK) return st;
   pkv::DecodeArgs a{};
   const CacheMaps* maps = nullptr;
@@ -327,8 +340,8 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
     a.out = out;
     a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
     a.err = ds->err;
-    plan_splits(num_seqs, num_kv_heads, max_blocks_per_seq, ds->num_sms, &a.split_tokens,
-                &a.max_splits);
+    pkv::plan_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, ds->num_sms,
+                            &a.split_tokens, &a.max_splits);
     if (a.max_splits > 1) {
       st = ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, a.max_splits));
       if (st != PKV_OK) return st;
@@ -351,9 +364,9 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
                                  int32_t num_seqs, int64_t total_q, int32_t num_q_heads,
                                  int32_t num_kv_heads, int32_t head_dim, float scale, void* out,
                                  pkv_stream_t stream) {
-  pkv_status st = validate_attention(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
-                                     max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
-                                     num_kv_heads, head_dim, out);
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_cache, v_cache, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
   if (st != PKV_OK) return st;
   if (!cu_seqlens_q || total_q < 0 || total_q > 0x7FFFFFFF) return PKV_ERR_INVALID_ARG;
   pkv::PrefillArgs a{};
@@ -432,7 +445,7 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
   // The plan never uses more splits than one per 64 tokens of the longest context.
   const int max_splits = (max_blocks_per_seq * pkv::kBlockSize + 63) / 64;
   int split_tokens = 0, splits = 0;
-  plan_splits(num_seqs, 1, max_blocks_per_seq, ds->num_sms, &split_tokens, &splits);
+  pkv::plan_decode_splits(num_seqs, 1, max_blocks_per_seq, ds->num_sms, &split_tokens, &splits);
   (void)max_splits;
   return ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, splits));
 }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 struct DeviceError;
@@ -86,6 +88,25 @@ cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream);
+
+// Helpers shared by the C entry points (defined in pkv_api.cu).
+// Split-K plan of a decode batch: tokens per context range and the number of
+// ranges of the longest possible sequence (max_blocks * 256 tokens).
+void plan_decode_splits(int num_seqs, int num_kv_heads, int max_blocks, int num_sms,
+                        int* split_tokens, int* max_splits);
+// Host-side shape, pointer and alignment checks of the attention calls.
+pkv_status validate_attention_args(const void* q, int64_t q_row_stride, const void* k_cache,
+                                   const void* v_cache, int64_t num_blocks,
+                                   const int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* lens, int32_t num_seqs, int32_t hq, int32_t hkv,
+                                   int32_t d, const void* out);
+// Resolves cuTensorMapEncodeTiled from the driver (once); false if unavailable.
+bool load_tensor_map_encoder();
+// Encodes the decode and prefill tensor maps of a cache (host only, no allocation).
+bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t num_blocks,
+                       int num_kv_heads, int head_dim);
+// Current bound on every in-kernel wait (pkv_set_wait_limit_ns).
+uint64_t wait_limit_ns();
 
 // Tensor-map encoder obtained from the driver at first use.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
