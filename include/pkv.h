@@ -114,11 +114,16 @@ pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
  * sequence with context 0 gets a zero output.  The context is split into
  * ranges processed in parallel (flash decoding; the number of ranges per
  * sequence is chosen from the batch shape and capped by pkv_set_max_splits)
- * and the partial results are merged by a log-sum-exp combine.  The partials
- * live in a library-owned workspace on the current device, allocated (and
- * grown) with cudaMalloc on first need; call pkv_reserve_workspace before
- * capturing this call in a CUDA graph.  Calls on different streams that
- * overlap share that workspace and must be serialised by the caller.
+ * and the partial results are merged by a log-sum-exp combine.  The
+ * sequences' contexts, laid end to end, are cut into equal slices, one per
+ * block of a grid that fills the GPU once (stream-K), so long and short
+ * contexts balance; only a context cut by a slice boundary is merged, by
+ * the block that finishes its last piece (one kernel launch in all).  The
+ * per-pair arrival counters and the partials live in a library-owned workspace
+ * on the current device, allocated (and grown) with cudaMalloc on first
+ * need; call pkv_reserve_workspace before capturing this call in a CUDA
+ * graph.  Calls on different streams that overlap share that workspace and
+ * must be serialised by the caller.
  */
 pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
                                 const void* v_cache, int64_t num_blocks,
@@ -171,20 +176,25 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
  * workspace.  The call itself calls no cudaMalloc, cudaFree or allocating
  * library routine.
  *
- * - Size limit: num_seqs * num_q_heads * splits * (head_dim + 2) * 4 bytes
- *   must fit in 16 MiB - 256 bytes, where splits is the plan's number of
- *   context ranges for a context of 256 * max_blocks_per_seq tokens (about
- *   148 * 16 / (num_seqs * num_kv_heads) ranges, capped by
- *   pkv_set_max_splits).  A batch that needs more returns
- *   PKV_ERR_UNSUPPORTED and launches nothing.  A plan of one range uses no
- *   scratch at all.
+ * - Size limit: the array holds a 256-byte error word, a 2 MiB region of
+ *   arrival counters (8 bytes per (sequence, KV head) pair, so at most
+ *   262144 pairs: num_seqs * num_kv_heads <= 262144) and the partials,
+ *   2 * B * G * (head_dim + 2) * 4 bytes, where G = num_q_heads /
+ *   num_kv_heads and B is the decode kernel's grid (the blocks that fit on
+ *   the GPU at once, a few per SM; at most num_seqs * num_kv_heads * cap
+ *   under pkv_set_max_splits(cap)), which must fit in the remaining
+ *   14 MiB - 256 bytes (a few MB on a 148-SM B300).  A
+ *   batch beyond either limit returns PKV_ERR_UNSUPPORTED and launches
+ *   nothing.
  * - Set-up: the first call on each device, with that device current, looks
  *   up the array's device address (cudaGetSymbolAddress); make that first
  *   call before any stream capture.
  * - Sharing: every call on a device uses the same array, which keeps the
- *   last call's contents (the kernels write every partial they read, so
- *   nothing needs clearing).  Calls whose kernels overlap on the GPU (on
- *   different streams without ordering) race on it: serialise them.
+ *   last call's contents.  Nothing needs clearing: the kernel writes every
+ *   partial it reads, and its arrival counters (zero at load) carry the
+ *   number of the call that wrote them, so older values count as zero.
+ *   Calls whose kernels overlap on the GPU (on different streams without
+ *   ordering) race on it: serialise them.
  * - Device-side checks still zero the output rows of out-of-range block ids
  *   or lengths, but their error code goes to a word inside the array and is
  *   not reported by pkv_get_device_error.
@@ -217,10 +227,12 @@ const char* pkv_version(void);
 pkv_status pkv_get_device_error(pkv_stream_t stream, int32_t* code, int32_t* info);
 
 /*
- * Cap the number of context ranges one sequence is split into by
- * pkv_decode_attention (0 = choose automatically, the default).  A larger
- * cap raises parallelism for few long sequences; the merge costs a little
- * extra memory traffic.  Process-wide.
+ * Cap the parallelism of pkv_decode_attention: with a cap n > 0 the decode
+ * grid has at most num_seqs * num_kv_heads * n blocks, so a context of
+ * average length is cut into at most about n + 1 pieces (0 = no cap, the
+ * default: the grid fills the GPU).  A larger cap raises parallelism for few
+ * long sequences; the merge costs a little extra memory traffic.
+ * Process-wide.
  */
 pkv_status pkv_set_max_splits(int32_t max_splits);
 
@@ -245,7 +257,7 @@ pkv_status pkv_set_wait_limit_ns(int64_t limit_ns);
  * Kernel timing: while enabled, every kernel launch of the library is
  * bracketed by CUDA events on its own stream.  pkv_profiler_read
  * synchronises the recorded events and returns, for kernel `name`
- * ("store_kvcache", "decode_split", "decode_combine", "prefill"), the summed
+ * ("store_kvcache", "decode", "prefill"), the summed
  * duration in milliseconds and the launch count since the last reset.
  */
 pkv_status pkv_profiler_enable(int32_t enable);

@@ -28,11 +28,16 @@
 
 namespace {
 
-// Size of the per-device scratch: the split-K partials of one call,
-// num_seqs * num_q_heads * splits * (head_dim + 2) fp32 values, after a
-// 256-byte word for the kernels' device-side error reports.
+// Layout of the per-device scratch: a 256-byte word for the kernels'
+// device-side error reports; the decode kernel's counters in a fixed region
+// of their own (zero at load, never reset, never overlapped by other data
+// whatever the batch shape): a 256-byte header with the launch epoch, then 8
+// bytes per (sequence, KV head) pair; then two partial slots per decode
+// block of G * (head_dim + 2) fp32 values.
 constexpr size_t kScratchBytes = size_t{16} << 20;
 constexpr size_t kErrBytes = 256;
+constexpr size_t kCounterBytes = (size_t{2} << 20) + 256;  // 262144 (sequence, KV head) pairs
+constexpr size_t kPartialBytes = kScratchBytes - kErrBytes - kCounterBytes;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
@@ -116,22 +121,19 @@ extern "C" pkv_status pkv_decode_attention_noalloc(
   a.out = out;
   a.wait_limit_ns = pkv::wait_limit_ns();
   a.err = reinterpret_cast<pkv::DeviceError*>(scratch);
-  pkv::plan_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, num_sms, &a.split_tokens,
-                          &a.max_splits);
-  if (a.max_splits > 1) {
-    // Partials of every (sequence, query head, range): head_dim + 2 fp32.
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * a.max_splits;
-    const size_t need = rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
-    if (need > kScratchBytes - kErrBytes) return PKV_ERR_UNSUPPORTED;
-    a.part_o = reinterpret_cast<float*>(scratch + kErrBytes);
-    a.part_ml = a.part_o + rows * head_dim;
-  }
+  const int g = num_q_heads / num_kv_heads;
+  const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  a.num_ctas = pkv::decode_num_ctas(head_dim, g, num_sms, pairs, pkv::max_splits_setting());
+  if (pkv::decode_counter_bytes(pairs) > kCounterBytes ||
+      pkv::decode_partial_bytes(a.num_ctas, g, head_dim) > kPartialBytes)
+    return PKV_ERR_UNSUPPORTED;
+  a.counters = reinterpret_cast<unsigned long long*>(scratch + kErrBytes);
+  a.part_o = reinterpret_cast<float*>(scratch + kErrBytes + kCounterBytes);
+  a.part_ml = a.part_o + static_cast<size_t>(a.num_ctas) * 2 * g * head_dim;
 
   pkv::CacheMaps maps;
   if (!pkv::encode_cache_maps(&maps, k_cache, v_cache, num_blocks, num_kv_heads, head_dim))
     return PKV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = pkv::launch_decode_split(a, maps, s);
-  if (e == cudaSuccess) e = pkv::launch_decode_combine(a, s);
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return pkv::launch_decode(a, maps, s) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -1,6 +1,7 @@
 // pkv_api.cu -- the extern "C" entry points of libpkv (declared in pkv.h):
 // host-side validation, per-device state (error word, decode workspace,
 // tensor-map cache), the split-K plan, and the kernel-timing profiler.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -34,8 +35,10 @@ struct DeviceState {
   bool usable = false;
   int num_sms = 0;
   DeviceError* err = nullptr;
-  float* ws = nullptr;
+  float* ws = nullptr;  // decode partials
   size_t ws_bytes = 0;
+  unsigned long long* cnt = nullptr;  // decode arrival counters (zeroed once)
+  size_t cnt_bytes = 0;
   MapEntry maps[kMapCacheSize];
   uint64_t clock = 0;
 };
@@ -172,49 +175,45 @@ const CacheMaps* cache_maps(DeviceState* ds, const void* k, const void* v, int64
 
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
 
-pkv_status ensure_workspace(DeviceState* ds, size_t bytes) {
-  if (bytes <= ds->ws_bytes) return PKV_OK;
-  if (ds->ws) cudaFree(ds->ws);
-  ds->ws = nullptr;
-  ds->ws_bytes = 0;
-  if (cudaMalloc(&ds->ws, bytes) != cudaSuccess) {
-    cudaGetLastError();
-    return PKV_ERR_NO_MEMORY;
+// Grows the decode partials to `part_bytes` and the counter region to
+// `cnt_bytes`.  The counters are zeroed when allocated and never reset
+// afterwards (the kernel tags them with a generation it keeps on the
+// device, so captured graphs replay correctly).
+pkv_status ensure_workspace(DeviceState* ds, size_t part_bytes, size_t cnt_bytes) {
+  if (part_bytes > ds->ws_bytes) {
+    if (ds->ws) cudaFree(ds->ws);
+    ds->ws = nullptr;
+    ds->ws_bytes = 0;
+    if (cudaMalloc(&ds->ws, part_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_NO_MEMORY;
+    }
+    ds->ws_bytes = part_bytes;
   }
-  ds->ws_bytes = bytes;
+  if (cnt_bytes > ds->cnt_bytes) {
+    if (ds->cnt) cudaFree(ds->cnt);
+    ds->cnt = nullptr;
+    ds->cnt_bytes = 0;
+    if (cudaMalloc(&ds->cnt, cnt_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_NO_MEMORY;
+    }
+    if (cudaMemset(ds->cnt, 0, cnt_bytes) != cudaSuccess) {
+      cudaFree(ds->cnt);
+      ds->cnt = nullptr;
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    ds->cnt_bytes = cnt_bytes;
+  }
   return PKV_OK;
-}
-
-size_t decode_ws_bytes(int num_seqs, int hq, int d, int max_splits) {
-  const size_t rows = static_cast<size_t>(num_seqs) * hq * max_splits;
-  return rows * d * sizeof(float) + rows * 2 * sizeof(float) + 256;
 }
 
 }  // namespace
 
 namespace pkv {
 
-// Split-K plan: enough (sequence, KV head, split) blocks to fill the GPU
-// several times over, splits a multiple of 64 tokens.
-void plan_decode_splits(int num_seqs, int hkv, int max_blocks, int num_sms, int* split_tokens,
-                        int* max_splits) {
-  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * kBlockSize;
-  const int64_t units = static_cast<int64_t>(num_seqs) * hkv;
-  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 16;
-  int64_t want = (target + units - 1) / units;
-  if (want < 1) want = 1;
-  int64_t split = (max_ctx + want - 1) / want;
-  split = ((split + 63) / 64) * 64;
-  const int cap = g_max_splits.load();
-  if (cap > 0) {
-    int64_t min_split = (max_ctx + cap - 1) / cap;
-    min_split = ((min_split + 63) / 64) * 64;
-    if (split < min_split) split = min_split;
-  }
-  if (split < 64) split = 64;
-  *split_tokens = static_cast<int>(split);
-  *max_splits = static_cast<int>((max_ctx + split - 1) / split);
-}
+int max_splits_setting() { return g_max_splits.load(); }
 
 // Tensor maps over the cache viewed as [slots][Hkv][D] (3-D: D, Hkv, slots).
 bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t num_blocks, int hkv,
@@ -340,21 +339,22 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
     a.out = out;
     a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
     a.err = ds->err;
-    pkv::plan_decode_splits(num_seqs, num_kv_heads, max_blocks_per_seq, ds->num_sms,
-                            &a.split_tokens, &a.max_splits);
-    if (a.max_splits > 1) {
-      st = ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, a.max_splits));
-      if (st != PKV_OK) return st;
-      a.part_o = ds->ws;
-      a.part_ml = ds->ws + static_cast<size_t>(num_seqs) * num_q_heads * a.max_splits * head_dim;
-    }
+    // Stream-K plan: one slice of the pairs' chunks per block; the workspace
+    // holds two partial slots per block, the counters one word per pair.
+    const int g = num_q_heads / num_kv_heads;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    a.num_ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
+                          pkv::decode_counter_bytes(pairs));
+    if (st != PKV_OK) return st;
+    a.counters = ds->cnt;
+    a.part_o = ds->ws;
+    a.part_ml = a.part_o + static_cast<size_t>(a.num_ctas) * 2 * g * head_dim;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const CacheMaps m = *maps;
-  cudaError_t e = timed_launch("decode_split", s, [&] { return pkv::launch_decode_split(a, m, s); });
-  if (e == cudaSuccess)
-    e = timed_launch("decode_combine", s, [&] { return pkv::launch_decode_combine(a, s); });
-  return cuda_status(e);
+  return cuda_status(
+      timed_launch("decode", s, [&] { return pkv::launch_decode(a, m, s); }));
 }
 
 pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void* k_cache,
@@ -442,12 +442,18 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
   pkv_status st;
   DeviceState* ds = device_state(&st);
   if (!ds) return st;
-  // The plan never uses more splits than one per 64 tokens of the longest context.
-  const int max_splits = (max_blocks_per_seq * pkv::kBlockSize + 63) / 64;
-  int split_tokens = 0, splits = 0;
-  pkv::plan_decode_splits(num_seqs, 1, max_blocks_per_seq, ds->num_sms, &split_tokens, &splits);
-  (void)max_splits;
-  return ensure_workspace(ds, decode_ws_bytes(num_seqs, num_q_heads, head_dim, splits));
+  // Worst case over the group sizes num_q_heads allows (the call does not
+  // name num_kv_heads).
+  size_t part = 0, cnt = 0;
+  for (int g = 1; g <= 16; g *= 2) {
+    if (num_q_heads % g) continue;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * (num_q_heads / g);
+    const int ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    part = std::max(part, pkv::decode_partial_bytes(ctas, g, head_dim));
+    cnt = std::max(cnt, pkv::decode_counter_bytes(pairs));
+  }
+  (void)max_blocks_per_seq;
+  return ensure_workspace(ds, part, cnt);
 }
 
 pkv_status pkv_set_wait_limit_ns(int64_t limit_ns) {

@@ -24,6 +24,7 @@ enum ErrSite : int {
   kSiteDecodeBlock = 201,
   kSiteDecodeWaitFull = 210,
   kSiteDecodeWaitEmpty = 211,
+  kSiteDecodeWaitMerge = 212,
   kSiteCombineContext = 220,
   kSitePrefillChunk = 300,
   kSitePrefillBlock = 301,
@@ -127,6 +128,34 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// Start pulling a tile of a tensor into L2 (no shared memory, no
+// completion): later loads of the tile hit L2.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1,
+                                                   int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Plain (non-tensor) bulk copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from global to this CTA's shared memory, completing on an
+// mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Barrier over the first `threads` threads of the block (named barrier `id`,
+// id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

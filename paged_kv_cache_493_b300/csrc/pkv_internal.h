@@ -40,11 +40,21 @@ struct DecodeArgs {
   int64_t num_blocks;
   float scale;
   void* out;
-  // split-K plan
-  int split_tokens;  // tokens per split (multiple of the chunk size)
-  int max_splits;    // splits of the longest possible sequence
-  float* part_o;     // [num_seqs][num_q_heads][max_splits][head_dim]
-  float* part_ml;    // [num_seqs][num_q_heads][max_splits][2]
+  // Stream-K plan: the (sequence, KV head) pairs' 32-token chunks, laid end
+  // to end, are cut into num_ctas equal slices, one per block.  A pair cut
+  // by a slice boundary leaves one partial state per piece; the block that
+  // writes the pair's last piece merges them.
+  int num_ctas;      // blocks of the decode kernel
+  // Counter region (zero when first used, never reset): a 256-byte header
+  // (word 0: launch epoch; word 1: blocks finished in this launch) and then
+  // one arrival counter per (sequence, KV head) pair, [num_seqs *
+  // num_kv_heads].  Every counter is tagged with the launch generation
+  // (epoch + 1, read by each block at its start; the last block to finish
+  // advances the epoch), so values left by earlier launches, even aborted
+  // ones or replays of the same captured graph, count as zero.
+  unsigned long long* counters;
+  float* part_o;     // [num_ctas][2][G][head_dim]
+  float* part_ml;    // [num_ctas][2][G][2] (running max, sum)
   uint64_t wait_limit_ns;
   DeviceError* err;
 };
@@ -81,19 +91,22 @@ constexpr int kDecodeChunk = 32;
 
 cudaError_t launch_store_kvcache(const StoreArgs& a, cudaStream_t stream);
 
-// Launches the split kernel and the combine kernel (profiled separately
-// through the callbacks in the API layer).
-cudaError_t launch_decode_split(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream);
-cudaError_t launch_decode_combine(const DecodeArgs& a, cudaStream_t stream);
+// Blocks of the decode kernel for a batch: as many as fit on the GPU at
+// once, at most num_pairs * max_splits when max_splits > 0.
+int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int max_splits);
+// Bytes of the decode kernel's arrival counters (zero when first used) and of
+// its partial slots.
+size_t decode_counter_bytes(int64_t num_pairs);
+size_t decode_partial_bytes(int num_ctas, int group, int head_dim);
+cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream);
 
 // Helpers shared by the C entry points (defined in pkv_api.cu).
-// Split-K plan of a decode batch: tokens per context range and the number of
-// ranges of the longest possible sequence (max_blocks * 256 tokens).
-void plan_decode_splits(int num_seqs, int num_kv_heads, int max_blocks, int num_sms,
-                        int* split_tokens, int* max_splits);
+// Process-wide cap on the number of pieces a pair is cut into
+// (pkv_set_max_splits; 0 = no cap).
+int max_splits_setting();
 // Host-side shape, pointer and alignment checks of the attention calls.
 pkv_status validate_attention_args(const void* q, int64_t q_row_stride, const void* k_cache,
                                    const void* v_cache, int64_t num_blocks,

@@ -6,15 +6,17 @@
 //
 // Pure data movement: each thread moves 16-byte vectors, several in flight
 // (all loads issued before any store), rows of K and V handled by the same
-// thread so that one slot lookup serves both.  Source rows are streamed
-// (no L1 allocation); destination writes go to L2 normally because the
-// attention kernel that follows reads them.
+// thread so that one slot lookup serves both.  The source loads do not wait
+// for the slot lookup (a source row is always in bounds), so the two
+// latencies overlap.  Source rows are streamed (no L1 allocation);
+// destination writes go to L2 normally because the attention kernel that
+// follows reads them.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
-constexpr int kStoreVecPerThread = 4;  // 16-byte vectors per tensor per thread
+constexpr int kStoreVecPerThread = 2;  // 16-byte vectors per tensor per thread
 constexpr int kStoreThreads = 256;
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -45,10 +47,10 @@ store_kvcache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
       const int64_t row = idx / row_vecs;
       const int col = static_cast<int>(idx - row * row_vecs);
       const int64_t slot = slot_mapping[row];
+      kv[j] = ld_stream(k + row * k_row_vecs + col);
+      vv[j] = ld_stream(v + row * v_row_vecs + col);
       if (slot >= 0 && slot < num_slots) {
         dst[j] = slot * row_vecs + col;
-        kv[j] = ld_stream(k + row * k_row_vecs + col);
-        vv[j] = ld_stream(v + row * v_row_vecs + col);
       } else if (slot != -1 && col == 0) {
         report_error(err, kErrDeviceCheck, kSiteStoreSlot);
       }

@@ -56,7 +56,7 @@ def test_knobs_validate_arguments(lib):
     assert lib.pkv_profiler_reset() == pkv.PKV_OK
     assert lib.pkv_reserve_workspace(4, 4, 96, 2) == pkv.PKV_ERR_INVALID_ARG
     ms, n = ctypes.c_double(), ctypes.c_int64()
-    assert lib.pkv_profiler_read(b"decode_split", ctypes.byref(ms), ctypes.byref(n)) == pkv.PKV_OK
+    assert lib.pkv_profiler_read(b"decode", ctypes.byref(ms), ctypes.byref(n)) == pkv.PKV_OK
     assert n.value == 0
     assert lib.pkv_profiler_read(None, ctypes.byref(ms), ctypes.byref(n)) == pkv.PKV_ERR_INVALID_ARG
 

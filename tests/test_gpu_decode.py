@@ -164,3 +164,61 @@ def test_strided_query_and_non_default_stream(cuda_device):
         pkv.pkv_decode_attention(q, kc, vc, bt, cl, case.scale, out, stream=s)
     s.synchronize()
     assert_close(out, oracle_decode_after_store(case), "strided q")
+
+
+def test_decode_call_finishes_promptly(cuda_device):
+    """A launch that only ends when a bounded wait expires still gives right
+    answers; this catches it by time (the 128-sequence batch takes well under a
+    millisecond on a B300, a drain or wait expiry takes a second or more)."""
+    import time
+    case = W.qwen_decode()
+    kc, vc, bt, cl = cache_to_device(case.cache)
+    q = dev(case.q)
+    out = torch.empty_like(q)
+    pkv.pkv_decode_attention(q, kc, vc, bt, cl, case.scale, out)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(5):
+        pkv.pkv_decode_attention(q, kc, vc, bt, cl, case.scale, out)
+    torch.cuda.synchronize()
+    assert (time.perf_counter() - t0) / 5 < 0.05
+    no_device_error()
+
+
+def test_graph_replays_follow_new_inputs(cuda_device):
+    """Store + decode captured once in a CUDA graph (as a serving engine
+    replays its decode step), then replayed over three different query
+    batches written into the captured buffers: every replay must give that
+    batch's attention.  Long contexts over a few pairs make the decode cut
+    every (sequence, KV head) context into several pieces, so each replay
+    goes through the cross-block merge and its arrival counters."""
+    case = W.make_decode_case("graph", [3000, 9000, 17, 5000], 16, 8, 128, 96, seed=511)
+    q, kc, vc, bt, cl = (dev(case.q), *cache_to_device(case.cache))
+    kn, vn, sm = dev(case.k_new), dev(case.v_new), dev(case.slot_mapping)
+    out = torch.empty_like(q)
+    pkv.pkv_reserve_workspace(case.num_seqs, 16, 128, bt.shape[1])
+
+    def step():
+        pkv.pkv_store_kvcache(kn, vn, sm, kc, vc)
+        pkv.pkv_decode_attention(q, kc, vc, bt, cl, case.scale, out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(77)
+    for i in range(3):
+        q_host = torch.randn(case.q.shape, generator=gen).to(torch.bfloat16)
+        q.copy_(q_host)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        replayed = W.DecodeCase(**{**case.__dict__, "q": q_host})
+        assert_close(out, oracle_decode_after_store(replayed), f"replay {i}")
+    no_device_error()

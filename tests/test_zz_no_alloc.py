@@ -37,8 +37,8 @@ def _within_tolerance(got, ref, what):
 def test_noalloc_matches_decode_on_two_calls_in_a_row(cuda_device):
     pkv.pkv_set_max_splits(0)
     pkv.pkv_set_wait_limit_ns(1_000_000_000)
-    # First call: a few long contexts (many splits per sequence); second call:
-    # the 128-sequence batch (a different split plan and partial layout), so
+    # First call: a few long contexts (each cut into many pieces); second
+    # call: the 128-sequence batch (another grid cut and partial layout), so
     # the second call runs over what the first left in the scratch.
     cases = [W.make_decode_case("na", [1, 300, 1500, 4000, 9000], 16, 8, 128, 64, seed=404,
                                 k_scale=3.0),
@@ -58,13 +58,12 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(cuda_device):
 
 
 def test_noalloc_rejects_a_batch_beyond_its_scratch(cuda_device):
-    """128 sequences x 16 query heads over one KV head with 128-block tables:
-    the plan asks for about 19 ranges per sequence, 38912 partial rows of
-    130 fp32 (20 MB), more than the 16 MiB array.  The call must refuse with
-    PKV_ERR_UNSUPPORTED and launch nothing.  (Every context is 1 token, so
-    even a launch would write no partials.)"""
+    """16400 sequences x 16 KV heads (head_dim 64, one query head per KV
+    head): 262400 (sequence, KV head) pairs, each needing an 8-byte arrival
+    counter, more than the array's 2 MiB counter region holds (262144).  The
+    call must refuse with PKV_ERR_UNSUPPORTED and launch nothing."""
     pkv.pkv_set_max_splits(0)
-    b, hq, hkv, d, mb = 128, 16, 1, 128, 128
+    b, hq, hkv, d, mb = 16400, 16, 16, 64, 1
     kc = torch.zeros(1, 256, hkv, d, dtype=torch.bfloat16, device="cuda")
     vc = torch.zeros_like(kc)
     q = torch.zeros(b, hq, d, dtype=torch.bfloat16, device="cuda")
