@@ -31,23 +31,28 @@
 // In one block:
 //   warp 4        producer: one lane walks the block's slice, looks up each
 //                 chunk's physical block, and issues TMA tile loads (K and V
-//                 rows of the KV head, 32 x head_dim bf16 each; with a
-//                 piece's first chunk also the G query rows) into a 4-stage
-//                 ring completing on mbarriers.  Each stage carries a
-//                 descriptor (sequence, KV head, slot, valid tokens, first /
-//                 last chunk of the piece); a final stage marks the end.
-//   warps 0..3    consumers: each takes a group of tokens of every chunk.
-//                 A lane owns head_dim/32 dimensions of the G query heads of
-//                 the group, so each K/V row loaded once from shared memory
-//                 serves all G query heads.  The G x T partial dot products of
-//                 a group (T = 16/G tokens) are reduced across the warp with a
-//                 butterfly in which every shuffle halves the values a lane
-//                 still holds (16 shuffles for 16 dot products instead of 80);
-//                 the slot order of the partials is permuted per lane so that
-//                 no selects are needed.  After the reduction lane l holds the
-//                 score of pair g(l) (twice: lanes l and l^1).  At the last
-//                 chunk of a piece the four warps merge their states and write
-//                 the output (a whole pair) or the piece's partials.
+//                 rows of the KV head, 32 tokens x 64 dimensions per panel,
+//                 128-byte swizzle; with a piece's first chunk also the G
+//                 query rows) into a 4-stage ring completing on mbarriers.
+//                 Each stage carries a descriptor (sequence, KV head, slot,
+//                 valid tokens, first / last chunk of the piece); a final
+//                 stage marks the end.
+//   warps 0..3    consumers: warp w computes the chunks c with c % 4 == w
+//                 (and reads every stage's descriptor).  A chunk is two
+//                 small contractions on the tensor cores (mma.sync m16n8k16,
+//                 bf16 in, fp32 accumulate): S^T = K q^T with the 32 tokens
+//                 as rows and the G query heads as columns (padded to 8), so
+//                 one K row fetched from shared memory serves the whole GQA
+//                 group; then O^T += V^T P^T with the head dimensions as rows.
+//                 The accumulator layout of S^T becomes the operand layout of
+//                 P^T by one 8x8 transpose in registers (movmatrix) per 16
+//                 tokens; the per-head running max is reduced over the eight
+//                 lanes that hold a head's tokens.  At the last chunk of a
+//                 piece the four warps merge their states and write the
+//                 output (a whole pair) or the piece's partials.
+// P is rounded to bf16 for the PV product (its sum l stays fp32).  V rows
+// past the context in a final, partial chunk are zeroed in shared memory
+// before the product (their pool contents may be anything).
 // The pipeline is HBM-bound: per token and KV head the kernel reads
 // 2 * head_dim * 2 bytes of K/V and does 4 * G * head_dim flops.
 #include <algorithm>
@@ -103,11 +108,16 @@ __device__ __forceinline__ unsigned long long tagged_increment(unsigned long lon
   return (atomicAdd(cnt, 1ull) & kCountMask) + 1;
 }
 
+constexpr int kPanelBytes = kDecodeChunk * 128;  // 32 rows x 64 dimensions (bf16)
+
+// Placed at a 1024-byte-aligned address (the 128-byte swizzle repeats every
+// 1024 bytes and the panels must start on that boundary).
 template <int D, int G>
 struct DecodeSmem {
-  alignas(128) __nv_bfloat16 k[kStages][kDecodeChunk][D];
-  alignas(128) __nv_bfloat16 v[kStages][kDecodeChunk][D];
-  alignas(128) __nv_bfloat16 q[kStages][G * D];
+  static constexpr int kPanels = D / 64;
+  uint8_t k[kStages][kPanels][kPanelBytes];
+  uint8_t v[kStages][kPanels][kPanelBytes];
+  alignas(16) __nv_bfloat16 q[kStages][G * D];
   float merge_o[kConsumerWarps][G][D];
   float merge_m[kConsumerWarps][G];
   float merge_l[kConsumerWarps][G];
@@ -125,23 +135,9 @@ struct DecodeSmem {
   int abort_flag;
 };
 
-// After the butterfly, lanes 2j and 2j+1 hold the score of pair j: at the
-// level that exchanges across lane bit b+1 the slots split on bit b.
-__device__ __forceinline__ int lane_of_pair(int j) { return j << 1; }
-
-template <int DPL>
-__device__ __forceinline__ void load_row(const __nv_bfloat16* row, int lane, float (&x)[DPL]) {
-  if constexpr (DPL == 4) {
-    const uint2 u = *reinterpret_cast<const uint2*>(row + lane * 4);
-    x[0] = bf16_lo(u.x);
-    x[1] = bf16_hi(u.x);
-    x[2] = bf16_lo(u.y);
-    x[3] = bf16_hi(u.y);
-  } else {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>(row + lane * 2);
-    x[0] = bf16_lo(u);
-    x[1] = bf16_hi(u);
-  }
+template <int D, int G>
+constexpr size_t decode_smem_bytes() {
+  return sizeof(DecodeSmem<D, G>) + 1024;  // slack for the 1024-byte alignment
 }
 
 // Chunks of each of sequence s's pairs: ceil(C / 32), and 1 for an empty
@@ -155,17 +151,16 @@ template <int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
-  constexpr int DPL = D / 32;          // dimensions per lane
-  constexpr int TW = kPairs / G;       // tokens per warp step
-  constexpr int LG = (G == 1) ? 0 : (G == 2) ? 1 : (G == 4) ? 2 : (G == 8) ? 3 : 4;
-  constexpr int GROUPS = kDecodeChunk / TW;  // warp steps per chunk
+  constexpr int kPanels = D / 64;
   constexpr uint32_t kChunkBytes = kDecodeChunk * D * 2;
   constexpr uint32_t kQBytes = G * D * 2;
   constexpr int kConsumerThreads = kConsumerWarps * 32;
   constexpr int kWarps = kDecodeThreads / 32;
 
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  DecodeSmem<D, G>& sm = *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t sraw = smem_u32(smem_raw);
+  DecodeSmem<D, G>& sm =
+      *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw + (((sraw + 1023u) & ~1023u) - sraw));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -316,8 +311,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             } else {
               const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
               mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u));
-              tma_load_3d(smem_u32(&sm.k[st][0][0]), &kmap, fb, 0, kvh, slot_row);
-              tma_load_3d(smem_u32(&sm.v[st][0][0]), &vmap, fb, 0, kvh, slot_row);
+#pragma unroll
+              for (int pn = 0; pn < kPanels; ++pn) {
+                tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
+                tma_load_3d(smem_u32(&sm.v[st][pn][0]), &vmap, fb, pn * 64, kvh, slot_row);
+              }
               if (k == k0)
                 bulk_load(smem_u32(&sm.q[st][0]),
                           static_cast<const __nv_bfloat16*>(a.q) +
@@ -355,29 +353,39 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int gl = lane >> 1;  // pair held by this lane after the butterfly
-    const int hl = gl & (G - 1);      // its head within the group
-    const int tl = gl >> LG;          // its token within the step
+    constexpr int NT = (G + 7) / 8;  // n-tiles of 8 query heads
+    constexpr int KS = D / 16;       // k-steps of S^T = K q^T; m-tiles of O^T
+    const int g = lane >> 2;         // fragment row group
+    const int cq = lane & 3;         // fragment column pair
+    const int li = lane >> 3, lr = lane & 7;  // ldmatrix: matrix and row this lane addresses
     const float qscale = a.scale * 1.4426950408889634f;
-    int rowoff[TW];
-#pragma unroll
-    for (int x = 0; x < TW; ++x) rowoff[x] = (x ^ tl) * D;
 
-    float qp[G][DPL];
-    float o[G][DPL];
-    float m_own = -INFINITY;  // running max of head hl (log2 domain)
-    float l_own = 0.f;        // running sum of this lane's pairs
+    uint32_t qb[KS][NT][2];  // q^T operand fragments: dims ks*16 + 2cq (+8), head nt*8 + g
+    float o[KS][NT][4];      // O^T: dims md*16 + g (+8), heads nt*8 + 2cq (+1)
+    float m_run[NT][2];      // running max of heads nt*8 + 2cq + j (log2 domain)
+    float l_run[NT][2];      // this lane's share of their running sums
     bool piece_bad = false;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) qp[hh][d] = o[hh][d] = 0.f;
+      for (int j = 0; j < 2; ++j) {
+        m_run[nt][j] = -INFINITY;
+        l_run[nt][j] = 0.f;
+      }
+#pragma unroll
+    for (int md = 0; md < KS; ++md)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        qb[md][nt][0] = qb[md][nt][1] = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[md][nt][e] = 0.f;
+      }
 
     int pieces_done = 0;  // pieces this block's consumers have merged
     for (int c = 0;; ++c) {
       const int st = c % kStages;
-      // Every exit decision is taken warp-uniformly (the shuffles below use
-      // the full mask).
+      // Every exit decision is taken warp-uniformly (the shuffles and the
+      // warp-wide matrix instructions below need the full warp).
       const bool got = mbar_wait(smem_u32(&sm.full[st]), (c / kStages) & 1, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
@@ -390,90 +398,141 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       const StageInfo inf = sm.info[st];
       if (inf.flags & kEnd) break;
       if (inf.flags & kFirst) {
-        m_own = -INFINITY;
-        l_own = 0.f;
         piece_bad = false;
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) o[hh][d] = 0.f;
+          for (int j = 0; j < 2; ++j) {
+            m_run[nt][j] = -INFINITY;
+            l_run[nt][j] = 0.f;
+          }
+#pragma unroll
+        for (int md = 0; md < KS; ++md)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[md][nt][e] = 0.f;
         if (inf.n_valid > 0) {
-          // q of the G heads for this lane's dimensions, permuted by hl so
-          // that slot x*G + hh multiplies head hh ^ hl.
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float x[DPL];
-            load_row<DPL>(&sm.q[st][(hh ^ hl) * D], lane, x);
+          for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + g;
 #pragma unroll
-            for (int d = 0; d < DPL; ++d) qp[hh][d] = x[d] * qscale;
+            for (int ks = 0; ks < KS; ++ks) {
+              const __nv_bfloat16* qr = &sm.q[st][h * D + ks * 16 + 2 * cq];
+              qb[ks][nt][0] = h < G ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+              qb[ks][nt][1] = h < G ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+            }
           }
         }
       }
       piece_bad |= (inf.flags & kBad) != 0;
       const int valid = inf.n_valid;
-      const __nv_bfloat16* kb = &sm.k[st][0][0];
-      const __nv_bfloat16* vb = &sm.v[st][0][0];
-#pragma unroll 1
-      for (int grp = warp; grp < GROUPS; grp += kConsumerWarps) {
-        const int t0 = grp * TW;
-        const int nv = valid - t0;
-        if (nv <= 0) break;
-        // ---- partial dot products, slot x*G + hh = pair ((x^tl)*G + (hh^hl))
-        float acc[kPairs];
+      bool zeroed = false;
+      if ((c % kConsumerWarps) == warp && valid > 0) {
+        const uint32_t kb = smem_u32(&sm.k[st][0][0]);
+        const uint32_t vb = smem_u32(&sm.v[st][0][0]);
+        if (valid < kDecodeChunk) {
+          // V rows past the context: zero them (pool contents may be
+          // anything, and 0 x NaN would poison the product).
+          for (int i = lane; i < (kDecodeChunk - valid) * 8 * kPanels; i += 32) {
+            const int pn = i % kPanels;
+            const int rest = i / kPanels;
+            *reinterpret_cast<uint4*>(&sm.v[st][pn][(valid + rest / 8) * 128 + (rest % 8) * 16]) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+          zeroed = true;
+        }
+        // ---- S^T = K q^T: two m-tiles of 16 tokens x NT n-tiles of 8 heads
+        float sc[2][NT][4];
 #pragma unroll
-        for (int x = 0; x < TW; ++x) {
-          float kx[DPL];
-          load_row<DPL>(kb + t0 * D + rowoff[x], lane, kx);
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float s = qp[hh][0] * kx[0];
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int d = 1; d < DPL; ++d) s = fmaf(qp[hh][d], kx[d], s);
-            acc[x * G + hh] = s;
+            for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            uint32_t af[4];
+            ldsm_x4(kb + (ks >> 2) * kPanelBytes +
+                        sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
+                    af);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
           }
         }
-        // ---- butterfly: each level keeps the lower half of the slots
+        // ---- online softmax per head (a head's 32 scores sit in the lanes
+        // with the same cq: two per m-tile in each of the 8 row groups)
+        float alpha[NT][2];
 #pragma unroll
-        for (int half = 8, mask = 16; half >= 1; half >>= 1, mask >>= 1) {
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-          for (int i = 0; i < half; ++i)
-            acc[i] += __shfl_xor_sync(0xffffffffu, acc[i + half], mask);
+          for (int j = 0; j < 2; ++j) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int tok = mt * 16 + hf * 8 + g;
+                const float x = tok < valid ? sc[mt][nt][hf * 2 + j] * qscale : -INFINITY;
+                sc[mt][nt][hf * 2 + j] = x;
+                mx = fmaxf(mx, x);
+              }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[nt][j], mx);  // finite: valid > 0
+            alpha[nt][j] = fast_exp2(m_run[nt][j] - m_new);
+            m_run[nt][j] = m_new;
+            float ls = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const float pv = fast_exp2(sc[mt][nt][hf * 2 + j] - m_new);
+                sc[mt][nt][hf * 2 + j] = pv;
+                ls += pv;
+              }
+            l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + ls;
+          }
         }
-        float s = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 1);
-        if (tl >= nv) s = -INFINITY;
-        // ---- online softmax per head (max over the token bits of the lane id)
-        float tm = s;
 #pragma unroll
-        for (int b = LG + 1; b <= 4; ++b)
-          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1 << b));
-        const float m_new = fmaxf(m_own, tm);
-        const float alpha_own = fast_exp2(m_own - m_new);
-        const float p = fast_exp2(s - m_new);
-        l_own = l_own * alpha_own + p;
-        m_own = m_new;
+        for (int md = 0; md < KS; ++md)
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const float al = __shfl_sync(0xffffffffu, alpha_own, lane_of_pair(hh));
+          for (int nt = 0; nt < NT; ++nt) {
+            o[md][nt][0] *= alpha[nt][0];
+            o[md][nt][1] *= alpha[nt][1];
+            o[md][nt][2] *= alpha[nt][0];
+            o[md][nt][3] *= alpha[nt][1];
+          }
+        // ---- P^T operand fragments: the S^T accumulator of tokens
+        // mt*16 + (0..7 | 8..15) is an 8x8 bf16 matrix per lane pair of
+        // columns; its transpose is the operand layout.
+        uint32_t pb[2][NT][2];
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) o[hh][d] *= al;
-        }
-        // ---- o += p V over the step's tokens
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int x = 0; x < TW; ++x) {
-          float pv[G];
+          for (int nt = 0; nt < NT; ++nt) {
+            pb[mt][nt][0] = movmatrix_trans(pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
+            pb[mt][nt][1] = movmatrix_trans(pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
+          }
+        // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, two k-steps of 16 tokens
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh)
-            pv[hh] = __shfl_sync(0xffffffffu, p, lane_of_pair(x * G + hh));
-          if (x < nv) {
-            float vx[DPL];
-            load_row<DPL>(vb + (t0 + x) * D, lane, vx);
+        for (int kt = 0; kt < 2; ++kt) {
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh)
+          for (int md = 0; md < KS; ++md) {
+            uint32_t af[4];
+            ldsm_x4_trans(vb + (md >> 2) * kPanelBytes +
+                              sw128_offset(kt * 16 + (li >> 1) * 8 + lr, (md & 3) * 2 + (li & 1)),
+                          af);
 #pragma unroll
-              for (int d = 0; d < DPL; ++d) o[hh][d] = fmaf(pv[hh], vx[d], o[hh][d]);
+            for (int nt = 0; nt < NT; ++nt) mma_16816(o[md][nt], af, pb[kt][nt][0], pb[kt][nt][1]);
           }
         }
       }
+      if (zeroed) fence_proxy_async_smem();  // generic writes before the next TMA into the stage
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
 
@@ -481,11 +540,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         // ---- merge the four warps' states and write the piece's result.
         // The hand-over between the warps uses mbarriers with bounded waits
         // (not bar.sync), so a warp that gave up cannot strand the others.
-        // l_own summed over the lanes of the same head (token bits only;
-        // lanes l and l^1 hold duplicates).
-        float l_sum = l_own;
+        // A head's sum: this lane's share added over the 8 row groups.
+        float l_sum[NT][2];
 #pragma unroll
-        for (int b = LG + 1; b <= 4; ++b) l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 1 << b);
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            float x = l_run[nt][j];
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            l_sum[nt][j] = x;
+          }
         const int k = pieces_done++;
         const bool freed = k == 0 || mbar_wait(smem_u32(&sm.merge_free), (k - 1) & 1,
                                                a.wait_limit_ns);
@@ -496,14 +562,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           }
           break;
         }
-        if ((lane & 1) == 0 && tl == 0) {
-          sm.merge_m[warp][hl] = m_own;
-          sm.merge_l[warp][hl] = l_sum;
-        }
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) sm.merge_o[warp][hh][lane * DPL + d] = o[hh][d];
+          for (int j = 0; j < 2; ++j) {
+            const int h = nt * 8 + 2 * cq + j;
+            if (g == 0 && h < G) {
+              sm.merge_m[warp][h] = m_run[nt][j];
+              sm.merge_l[warp][h] = l_sum[nt][j];
+            }
+          }
+#pragma unroll
+        for (int md = 0; md < KS; ++md)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = nt * 8 + 2 * cq + (e & 1);
+              if (h < G) sm.merge_o[warp][h][md * 16 + g + (e >> 1) * 8] = o[md][nt][e];
+            }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.merge_full));
         const bool merged = mbar_wait(smem_u32(&sm.merge_full), k & 1, a.wait_limit_ns);
@@ -625,7 +702,7 @@ template <int D, int G>
 int ctas_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
-    const size_t smem = sizeof(DecodeSmem<D, G>);
+    const size_t smem = decode_smem_bytes<D, G>();
     auto kern = decode_split_kernel<D, G>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -653,7 +730,7 @@ int ctas_per_sm_d(int group) {
 
 template <int D, int G>
 cudaError_t launch_split_t(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream) {
-  const size_t smem = sizeof(DecodeSmem<D, G>);
+  const size_t smem = decode_smem_bytes<D, G>();
   auto kern = decode_split_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

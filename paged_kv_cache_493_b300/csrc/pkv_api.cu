@@ -221,10 +221,10 @@ bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t nu
   const uint64_t slots = static_cast<uint64_t>(num_blocks) * kBlockSize;
   const uint64_t s1 = static_cast<uint64_t>(d) * 2;
   const uint64_t s2 = static_cast<uint64_t>(hkv) * d * 2;
-  return encode_3d(&maps->k_rows, k, d, hkv, slots, s1, s2, d, 1, kDecodeChunk,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         encode_3d(&maps->v_rows, v, d, hkv, slots, s1, s2, d, 1, kDecodeChunk,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
+  return encode_3d(&maps->k_rows, k, d, hkv, slots, s1, s2, 64, 1, kDecodeChunk,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
+         encode_3d(&maps->v_rows, v, d, hkv, slots, s1, s2, 64, 1, kDecodeChunk,
+                   CU_TENSOR_MAP_SWIZZLE_128B) &&
          encode_3d(&maps->k_sw128, k, d, hkv, slots, s1, s2, 64, 1, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
          encode_3d(&maps->v_sw128, v, d, hkv, slots, s1, s2, 64, 1, 128,

@@ -80,7 +80,7 @@ struct PrefillArgs {
 
 // Tensor maps built by the API layer (cached per cache pointer).
 struct CacheMaps {
-  CUtensorMap k_rows;   // decode: box {head_dim, 1, 32} over [slots][Hkv][D]
+  CUtensorMap k_rows;   // decode: box {64, 1, 32} over [slots][Hkv][D], 128-byte swizzle
   CUtensorMap v_rows;
   CUtensorMap k_sw128;  // prefill: box {64, 1, 128}, 128-byte swizzle
   CUtensorMap v_sw128;
