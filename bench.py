@@ -49,6 +49,11 @@ from paged_kv_cache_493_b300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of HBM peak) and decode tokens/s/layer"
 MAIN_WORKLOAD = "qwen_decode_b128"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# DRAM bytes (read + write) of one decode_split launch on qwen_decode_b128,
+# from the ncu capture summarised in profiles/decode_split_qwen_decode_b128.md.
+# Valid only for the kernel version that capture measured: set to None when
+# the kernel changes, until it is captured again.
+DECODE_SPLIT_TRAFFIC_BYTES = 328.7e6
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -384,7 +389,7 @@ def run_gpu(args, rank, world, local):
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": None,
+            "traffic": DECODE_SPLIT_TRAFFIC_BYTES,
             "algorithmic_bytes_per_launch": bytes_["split_kernel"],
             "avg_launch_ms": round(split_ms, 5),
             "kernel_ms": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},

@@ -65,8 +65,11 @@ namespace pkv {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarps = 4;  // warps 0..3: warp w computes the chunks c with c % 4 == w
+constexpr int kProducerWarp = 4;   // TMA issue
+constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
+constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum-exp over L2)
+constexpr int kDecodeThreads = 7 * 32;
 constexpr int kPairs = 16;  // (token, head) dot products per warp step
 
 // Descriptor of one ring stage, written by the producer before it arrives
@@ -102,10 +105,25 @@ constexpr int kPairCounterOffset = 256 / sizeof(unsigned long long);  // after t
 // plain atomics and no compare-and-swap loop, so many blocks arriving at
 // once do not retry: the max lifts a counter of an older generation to
 // (gen, 0) and leaves one of this generation alone; the add then counts.
+// The add has acquire-release semantics at GPU scope: the caller's earlier
+// writes (and those of its warp, ordered by a preceding __syncwarp) are
+// visible to whoever observes the count, and the caller sees what the
+// earlier arrivals wrote.
 __device__ __forceinline__ unsigned long long tagged_increment(unsigned long long* cnt,
                                                                unsigned long long gen) {
   atomicMax(cnt, gen << kCountBits);
-  return (atomicAdd(cnt, 1ull) & kCountMask) + 1;
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(cnt), "l"(1ull)
+               : "memory");
+  return (old & kCountMask) + 1;
+}
+
+// Acquire-release fence at GPU scope (lighter than the sequentially
+// consistent __threadfence).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
 constexpr int kPanelBytes = kDecodeChunk * 128;  // 32 rows x 64 dimensions (bf16)
@@ -118,20 +136,27 @@ struct DecodeSmem {
   uint8_t k[kStages][kPanels][kPanelBytes];
   uint8_t v[kStages][kPanels][kPanelBytes];
   alignas(16) __nv_bfloat16 q[kStages][G * D];
-  float merge_o[kConsumerWarps][G][D];
-  float merge_m[kConsumerWarps][G];
-  float merge_l[kConsumerWarps][G];
+  // Mailbox from the consumer warps to the merger: each warp's state of a
+  // finished piece.
+  alignas(16) float mail_o[kConsumerWarps][G][D];
+  float mail_m[kConsumerWarps][G];
+  float mail_l[kConsumerWarps][G];
+  StageInfo mail_info;
   StageInfo info[kStages];
   long long scan[kDecodeThreads / 32];
   long long start_base;  // chunk offset (per KV head) of the slice's first sequence
+  long long end_base;    // ... and of the sequence of its last chunk
   unsigned long long gen;  // this launch's generation (counter tag)
-  StageInfo merge_todo[2];  // cut pairs whose last piece this block wrote
-  int n_merge;
   int start_seq;
+  int end_seq;
   alignas(8) uint64_t full[kStages];
   alignas(8) uint64_t empty[kStages];
-  alignas(8) uint64_t merge_full;  // the four warps' piece states are in merge_*
-  alignas(8) uint64_t merge_free;  // ... and have been read
+  alignas(8) uint64_t mail_full;  // the consumer warps' states are posted
+  alignas(8) uint64_t mail_free;  // ... and have been taken by the merger
+  // Merge jobs for the merge warp: a block holds at most two cut pieces, so
+  // at most two merges and then an end marker; each slot is used once.
+  StageInfo job[3];
+  alignas(8) uint64_t job_full[3];
   int abort_flag;
 };
 
@@ -147,14 +172,143 @@ __device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int max_ct
   return (ctx <= 0 || ctx > max_ctx) ? 1 : (ctx + kDecodeChunk - 1) / kDecodeChunk;
 }
 
+// The partial slot of the piece of a cut pair held by block cb2 (the pair
+// spans blocks c_first .. c_last; only blocks with a non-empty slice hold a
+// piece).
+__device__ __forceinline__ int64_t piece_row(const StageInfo& inf, int cb2, int G) {
+  const int sl = cb2 == inf.c_first ? inf.first_slot : 0;
+  return (static_cast<int64_t>(cb2) * 2 + sl) * G;
+}
+
+// Merge of all pieces of a cut pair by one warp (log-sum-exp):
+//   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
+// Pieces go to lanes in batches of 32, so every load of a pass is
+// independent of the others: lane j reads piece j's (m, l), the warp
+// reduces M and L, and the weights w_j = 2^(m_j - M) / L are broadcast by
+// shuffle while each lane accumulates its own dimensions.
 template <int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads)
+__device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long T, long long nb,
+                           int64_t row_base, int lane) {
+  const int n = inf.c_last - inf.c_first + 1;  // blocks spanned (empty ones hold no piece)
+  if (n <= 32) {
+    // Lane j holds piece j's (m, l) for every head: one round of loads.
+    const int cb2 = inf.c_first + lane;
+    const bool has = lane < n && slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
+    const int64_t r = has ? piece_row(inf, cb2, G) : 0;
+    float w[G], inv[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float m = has ? __ldcg(a.part_ml + (r + h) * 2) : -INFINITY;
+      const float l = has ? __ldcg(a.part_ml + (r + h) * 2 + 1) : 0.f;
+      float M = m;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = (has && M != -INFINITY) ? fast_exp2(m - M) : 0.f;
+      float L = l * f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const bool bad = __any_sync(0xffffffffu, l < 0.f);
+      inv[h] = (L > 0.f && !bad) ? 1.f / L : 0.f;
+      w[h] = f;
+    }
+    // Lane = dimension: every piece's rows of every head, loads independent
+    // of each other (an empty block's weight is 0 and its slot is selected
+    // away, never multiplied).
+    float acc[G][D / 32];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc[h][i] = 0.f;
+#pragma unroll 2
+    for (int j = 0; j < n; ++j) {
+      const int64_t rj = piece_row(inf, inf.c_first + j, G);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float wj = __shfl_sync(0xffffffffu, w[h], j);
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const float x = __ldcg(a.part_o + (rj + h) * D + i * 32 + lane);
+          acc[h][i] += wj != 0.f ? wj * x : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i)
+        static_cast<__nv_bfloat16*>(a.out)[(row_base + h) * D + i * 32 + lane] =
+            __float2bfloat16_rn(acc[h][i] * inv[h]);
+    return;
+  }
+  for (int h = 0; h < G; ++h) {
+    // pass 1: M and the bad flag, then L (lane j: piece j of a batch of 32)
+    float M = -INFINITY;
+    bool bad = false;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int cb2 = inf.c_first + j0 + lane;
+      const bool has = j0 + lane < n && slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
+      const int64_t r = has ? piece_row(inf, cb2, G) + h : 0;
+      M = fmaxf(M, has ? __ldcg(a.part_ml + r * 2) : -INFINITY);
+      bad |= has && __ldcg(a.part_ml + r * 2 + 1) < 0.f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    bad = __any_sync(0xffffffffu, bad);
+    float L = 0.f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int cb2 = inf.c_first + j0 + lane;
+      const bool has = j0 + lane < n && slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
+      const int64_t r = has ? piece_row(inf, cb2, G) + h : 0;
+      if (has && M != -INFINITY)
+        L += __ldcg(a.part_ml + r * 2 + 1) * fast_exp2(__ldcg(a.part_ml + r * 2) - M);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+    // pass 2: out[d] = sum_j w_j o_j[d], weights broadcast by shuffle
+    float acc[D / 32];
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int cb2 = inf.c_first + j0 + lane;
+      const bool has = j0 + lane < n && slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
+      const float w = (has && M != -INFINITY)
+                          ? fast_exp2(__ldcg(a.part_ml + (piece_row(inf, cb2, G) + h) * 2) - M)
+                          : 0.f;
+      const int cnt = min(32, n - j0);
+#pragma unroll 4
+      for (int j = 0; j < cnt; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j);
+        const int64_t r = piece_row(inf, inf.c_first + j0 + j, G) + h;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const float x = __ldcg(a.part_o + r * D + i * 32 + lane);
+          acc[i] += wj != 0.f ? wj * x : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i)
+      static_cast<__nv_bfloat16*>(a.out)[(row_base + h) * D + i * 32 + lane] =
+          __float2bfloat16_rn(acc[i] * inv);
+  }
+}
+
+// Two blocks per SM (measured best for the HBM-bound decode: more, shorter
+// slices cost more cut contexts than the extra streams gain) need at most
+// 65536 / (2 * 224) registers per thread.
+template <int G>
+constexpr int decode_max_regs() {
+  return G <= 8 ? 128 : 255;
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<G>())
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
   constexpr int kPanels = D / 64;
   constexpr uint32_t kChunkBytes = kDecodeChunk * D * 2;
   constexpr uint32_t kQBytes = G * D * 2;
-  constexpr int kConsumerThreads = kConsumerWarps * 32;
   constexpr int kWarps = kDecodeThreads / 32;
 
   extern __shared__ uint8_t smem_raw[];
@@ -170,15 +324,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kConsumerWarps);
     }
-    mbar_init(smem_u32(&sm.merge_full), kConsumerWarps);
-    mbar_init(smem_u32(&sm.merge_free), kConsumerWarps);
+    mbar_init(smem_u32(&sm.mail_full), kConsumerWarps);
+    mbar_init(smem_u32(&sm.mail_free), 1);
+    for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&sm.job_full[j]), 1);
     sm.abort_flag = 0;
-    sm.n_merge = 0;
     sm.start_seq = -1;
     sm.start_base = 0;
+    sm.end_seq = -1;
+    sm.end_base = 0;
     fence_barrier_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
@@ -189,9 +345,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 
   const int max_ctx = a.max_blocks * kBlockSize;
   const int hkv = a.num_kv_heads;
-  // The epoch changes only after every block of this launch has passed this
-  // point (the last block to finish advances it), so all blocks agree.
-  if (threadIdx.x == 0) sm.gen = ((__ldcg(a.counters) + 1) & kGenMask);
+  // Launch generation: epoch + 1.  Each block reads the epoch, then counts
+  // itself on the start counter; the block that completes the count (so
+  // every block has read the epoch) advances the epoch for the next launch,
+  // which cannot start before this one ends.  Off the critical path: the
+  // atomics overlap the rest of the block's work.
+  if (threadIdx.x == 0) {
+    const unsigned long long gen = (__ldcg(a.counters) + 1) & kGenMask;
+    sm.gen = gen;
+    if (tagged_increment(a.counters + 1, gen) == gridDim.x)
+      atomicExch(a.counters, gen);  // epoch := generation
+  }
 
   // ---- prefix sums of the chunk counts over the sequences (whole block):
   // thread t owns sequences [seg0, seg1).
@@ -219,6 +383,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   const long long nb = gridDim.x;
   const long long ca = static_cast<long long>(blockIdx.x) * T / nb;        // slice begin
   const long long cb = (static_cast<long long>(blockIdx.x) + 1) * T / nb;  // slice end
+  // The sequences holding the slice's first and last chunks.
   if (ca < cb && ca >= excl * hkv && ca < (excl + mine) * hkv) {
     long long p = excl;
     for (int s = seg0; s < seg1; ++s) {
@@ -231,9 +396,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       p += n;
     }
   }
+  if (ca < cb && cb - 1 >= excl * hkv && cb - 1 < (excl + mine) * hkv) {
+    long long p = excl;
+    for (int s = seg0; s < seg1; ++s) {
+      const int n = seq_chunks(a, s, max_ctx);
+      if (cb - 1 < (p + n) * hkv) {
+        sm.end_seq = s;
+        sm.end_base = p;
+        break;
+      }
+      p += n;
+    }
+  }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // Last post of each stage (copies or descriptor only): phases of one
@@ -255,8 +432,85 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         return *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0;
       };
 
+      // Emits the chunks [pos, piece_end) of one piece of sequence pseq (its
+      // pairs start at chunk pbase, pnch chunks each); false on abort.
+      auto emit_piece = [&](int pseq, long long pbase, int pctx, bool pbad_ctx, int pnch,
+                            long long pos, long long piece_end, int slot) -> bool {
+        const int kvh = static_cast<int>((pos - pbase) / pnch);
+        const int k0 = static_cast<int>((pos - pbase) % pnch);
+        const long long pair_end = pbase + static_cast<long long>(kvh + 1) * pnch;
+        const int n = static_cast<int>(piece_end - pos);
+        const bool whole = k0 == 0 && piece_end == pair_end;
+        const long long pair_begin = pair_end - pnch;
+        const int c_first = block_of_chunk(pair_begin, T, nb);
+        const int c_last = block_of_chunk(pair_end - 1, T, nb);
+        const int first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
+        const int32_t* table = a.block_tables + static_cast<int64_t>(pseq) * a.max_blocks;
+        for (int k = k0; k < k0 + n; ++k, ++c) {
+          const int st = c % kStages;
+          if (!claim(st)) return false;
+          const int tok = k * kDecodeChunk;
+          const int n_valid = (pbad_ctx || pctx <= 0) ? 0 : min(kDecodeChunk, pctx - tok);
+          int id = 0;
+          bool bad = pbad_ctx;
+          if (n_valid > 0) {
+            id = table[tok >> 8];
+            if (id < 0 || id >= a.num_blocks) {
+              bad = true;
+              report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
+            }
+          }
+          StageInfo& inf = sm.info[st];
+          inf.seq = pseq;
+          inf.kvh = kvh;
+          inf.slot = slot;
+          inf.n_valid = bad ? 0 : n_valid;
+          inf.flags = (bad ? kBad : 0) | (whole ? kSingle : 0) | (k == k0 ? kFirst : 0) |
+                      (k == k0 + n - 1 ? kLast : 0);
+          inf.c_first = c_first;
+          inf.c_last = c_last;
+          inf.first_slot = first_slot;
+          const uint32_t fb = smem_u32(&sm.full[st]);
+          last_posted[st] = c;
+          if (inf.n_valid <= 0) {
+            mbar_arrive(fb);  // descriptor only
+          } else {
+            const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
+            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u));
+#pragma unroll
+            for (int pn = 0; pn < kPanels; ++pn) {
+              tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
+              tma_load_3d(smem_u32(&sm.v[st][pn][0]), &vmap, fb, pn * 64, kvh, slot_row);
+            }
+            if (k == k0)
+              bulk_load(smem_u32(&sm.q[st][0]),
+                        static_cast<const __nv_bfloat16*>(a.q) +
+                            static_cast<int64_t>(pseq) * a.q_row_stride +
+                            static_cast<int64_t>(kvh) * G * D,
+                        kQBytes, fb);
+          }
+        }
+        return true;
+      };
+
       int seq = sm.start_seq;
       if (ca < cb && seq >= 0) {
+        // A piece cut at the slice's end is processed first: its pair's
+        // cross-block merge then happens while the stream goes on, and the
+        // block ends on a piece that needs none.
+        long long stop = cb;
+        if (sm.end_seq >= 0) {
+          const int eseq = sm.end_seq;
+          const long long ebase = sm.end_base * hkv;
+          const int ectx = a.context_lens[eseq];
+          const int enc = seq_chunks(a, eseq, max_ctx);
+          const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
+          if (epair_begin + enc > cb && epair_begin > ca) {
+            if (!emit_piece(eseq, ebase, ectx, ectx < 0 || ectx > max_ctx, enc, epair_begin, cb, 1))
+              aborted = true;
+            stop = epair_begin;
+          }
+        }
         long long base = sm.start_base * hkv;  // first chunk of seq's pairs
         int ctx = a.context_lens[seq];
         bool ctx_bad = ctx < 0 || ctx > max_ctx;
@@ -264,69 +518,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
         int piece = 0;
-        while (pos < cb && !aborted) {
+        while (pos < stop && !aborted) {
           const int kvh = static_cast<int>((pos - base) / nch);
-          const int k0 = static_cast<int>((pos - base) % nch);
           const long long pair_end = base + static_cast<long long>(kvh + 1) * nch;
-          const long long piece_end = pair_end < cb ? pair_end : cb;
-          const int n = static_cast<int>(piece_end - pos);
-          const bool whole = k0 == 0 && piece_end == pair_end;
-          const int slot = piece == 0 ? 0 : 1;
-          const long long pair_begin = pair_end - nch;
-          const int c_first = block_of_chunk(pair_begin, T, nb);
-          const int c_last = block_of_chunk(pair_end - 1, T, nb);
-          const int first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
-          const int32_t* table = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
-          for (int k = k0; k < k0 + n; ++k, ++c) {
-            const int st = c % kStages;
-            if (!claim(st)) {
-              aborted = true;
-              break;
-            }
-            const int tok = k * kDecodeChunk;
-            const int n_valid = (ctx_bad || ctx <= 0) ? 0 : min(kDecodeChunk, ctx - tok);
-            int id = 0;
-            bool bad = ctx_bad;
-            if (n_valid > 0) {
-              id = table[tok >> 8];
-              if (id < 0 || id >= a.num_blocks) {
-                bad = true;
-                report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
-              }
-            }
-            StageInfo& inf = sm.info[st];
-            inf.seq = seq;
-            inf.kvh = kvh;
-            inf.slot = slot;
-            inf.n_valid = bad ? 0 : n_valid;
-            inf.flags = (bad ? kBad : 0) | (whole ? kSingle : 0) | (k == k0 ? kFirst : 0) |
-                        (k == k0 + n - 1 ? kLast : 0);
-            inf.c_first = c_first;
-            inf.c_last = c_last;
-            inf.first_slot = first_slot;
-            const uint32_t fb = smem_u32(&sm.full[st]);
-            last_posted[st] = c;
-            if (inf.n_valid <= 0) {
-              mbar_arrive(fb);  // descriptor only
-            } else {
-              const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
-              mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u));
-#pragma unroll
-              for (int pn = 0; pn < kPanels; ++pn) {
-                tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
-                tma_load_3d(smem_u32(&sm.v[st][pn][0]), &vmap, fb, pn * 64, kvh, slot_row);
-              }
-              if (k == k0)
-                bulk_load(smem_u32(&sm.q[st][0]),
-                          static_cast<const __nv_bfloat16*>(a.q) +
-                              static_cast<int64_t>(seq) * a.q_row_stride +
-                              static_cast<int64_t>(kvh) * G * D,
-                          kQBytes, fb);
-            }
+          const long long piece_end = pair_end < stop ? pair_end : stop;
+          if (!emit_piece(seq, base, ctx, ctx_bad, nch, pos, piece_end, piece == 0 ? 0 : 1)) {
+            aborted = true;
+            break;
           }
           pos = piece_end;
           ++piece;
-          if (pos == pair_end && kvh + 1 == hkv && pos < cb) {  // next sequence
+          if (pos == pair_end && kvh + 1 == hkv && pos < stop) {  // next sequence
             ++seq;
             base = pair_end;
             ctx = a.context_lens[seq];
@@ -351,7 +553,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         if (last_posted[s] >= 0)
           mbar_wait(smem_u32(&sm.full[s]), (last_posted[s] / kStages) & 1, kDrainLimitNs);
     }
-  } else {
+  } else if (warp < kConsumerWarps) {
     // ------------------------------------------------------------ consumers
     constexpr int NT = (G + 7) / 8;  // n-tiles of 8 query heads
     constexpr int KS = D / 16;       // k-steps of S^T = K q^T; m-tiles of O^T
@@ -366,22 +568,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     float l_run[NT][2];      // this lane's share of their running sums
     bool piece_bad = false;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        m_run[nt][j] = -INFINITY;
-        l_run[nt][j] = 0.f;
-      }
-#pragma unroll
     for (int md = 0; md < KS; ++md)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        qb[md][nt][0] = qb[md][nt][1] = 0u;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[md][nt][e] = 0.f;
-      }
+      for (int nt = 0; nt < NT; ++nt) qb[md][nt][0] = qb[md][nt][1] = 0u;
 
-    int pieces_done = 0;  // pieces this block's consumers have merged
+    int posts = 0;  // pieces (and the final end marker) posted to the merger
+    // Claims the mailbox (bounded wait for the merger to take the last post).
+    auto claim_mail = [&](int k) -> bool {
+      const bool ok = k < 1 || mbar_wait(smem_u32(&sm.mail_free), (k - 1) & 1, a.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
+          atomicExch(&sm.abort_flag, 1);
+        }
+        return false;
+      }
+      return true;
+    };
+    bool mail_ok = true;
     for (int c = 0;; ++c) {
       const int st = c % kStages;
       // Every exit decision is taken warp-uniformly (the shuffles and the
@@ -537,39 +741,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
 
       if (inf.flags & kLast) {
-        // ---- merge the four warps' states and write the piece's result.
-        // The hand-over between the warps uses mbarriers with bounded waits
-        // (not bar.sync), so a warp that gave up cannot strand the others.
-        // A head's sum: this lane's share added over the 8 row groups.
-        float l_sum[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float x = l_run[nt][j];
-            x += __shfl_xor_sync(0xffffffffu, x, 4);
-            x += __shfl_xor_sync(0xffffffffu, x, 8);
-            x += __shfl_xor_sync(0xffffffffu, x, 16);
-            l_sum[nt][j] = x;
-          }
-        const int k = pieces_done++;
-        const bool freed = k == 0 || mbar_wait(smem_u32(&sm.merge_free), (k - 1) & 1,
-                                               a.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, freed)) {
-          if (lane == 0) {
-            report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
-            atomicExch(&sm.abort_flag, 1);
-          }
+        // ---- post this warp's state of the piece (max, sum, unnormalised
+        // output) to the merger and go on with the next chunk at once.
+        const int k = posts++;
+        if (!claim_mail(k)) {
+          mail_ok = false;
           break;
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
+            float x = l_run[nt][j];  // a head's sum: this lane's share over the 8 row groups
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
             const int h = nt * 8 + 2 * cq + j;
             if (g == 0 && h < G) {
-              sm.merge_m[warp][h] = m_run[nt][j];
-              sm.merge_l[warp][h] = l_sum[nt][j];
+              sm.mail_m[warp][h] = m_run[nt][j];
+              sm.mail_l[warp][h] = x;
             }
           }
 #pragma unroll
@@ -579,122 +769,154 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int h = nt * 8 + 2 * cq + (e & 1);
-              if (h < G) sm.merge_o[warp][h][md * 16 + g + (e >> 1) * 8] = o[md][nt][e];
+              if (h < G) sm.mail_o[warp][h][md * 16 + g + (e >> 1) * 8] = o[md][nt][e];
             }
+        if (warp == 0 && lane == 0) {  // every warp saw the same descriptors
+          StageInfo post = inf;
+          post.flags = (inf.flags & ~kBad) | (piece_bad ? kBad : 0);
+          sm.mail_info = post;
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.merge_full));
-        const bool merged = mbar_wait(smem_u32(&sm.merge_full), k & 1, a.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, merged)) {
-          if (lane == 0) {
-            report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
-            atomicExch(&sm.abort_flag, 1);
-          }
-          break;
-        }
-        const int64_t row_base = static_cast<int64_t>(inf.seq) * a.num_q_heads + inf.kvh * G;
-        const int64_t prow = (static_cast<int64_t>(blockIdx.x) * 2 + inf.slot) * G;
-        for (int idx = threadIdx.x; idx < G * D; idx += kConsumerThreads) {
-          const int hh = idx / D;
-          const int d = idx - hh * D;
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.merge_m[w][hh]);
-          float L = 0.f, O = 0.f;
-          if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-              const float f = fast_exp2(sm.merge_m[w][hh] - M);
-              L += sm.merge_l[w][hh] * f;
-              O += sm.merge_o[w][hh][d] * f;
-            }
-          }
-          if (inf.flags & kSingle) {
-            const float r = (L > 0.f && !piece_bad) ? O / L : 0.f;
-            static_cast<__nv_bfloat16*>(a.out)[(row_base + hh) * D + d] = __float2bfloat16_rn(r);
-          } else {
-            a.part_o[(prow + hh) * D + d] = O;
-            if (d == 0) {
-              a.part_ml[(prow + hh) * 2 + 0] = M;
-              a.part_ml[(prow + hh) * 2 + 1] = piece_bad ? -1.f : L;
-            }
-          }
-        }
-        if (!(inf.flags & kSingle)) __threadfence();  // partials visible before the arrival
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.merge_free));
-        if (!(inf.flags & kSingle) && warp == 0) {
-          // ---- a cut pair: once all four warps have written the piece,
-          // count it on the pair's arrival counter; the block that brings
-          // the count to the pair's number of pieces merges them.
-          const bool all_written =
-              mbar_wait(smem_u32(&sm.merge_free), k & 1, a.wait_limit_ns);
-          if (!__all_sync(0xffffffffu, all_written)) {
-            if (lane == 0) {
-              report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
-              atomicExch(&sm.abort_flag, 1);
-            }
-            break;
-          }
-          // A block holds at most two cut pieces (the first and the last of
-          // its slice), so at most two merges land here; they run after
-          // the slice, with every thread of the block.
-          if (lane == 0) {
-            int pieces = 0;  // blocks with a non-empty slice in [c_first, c_last]
-            for (int cb2 = inf.c_first; cb2 <= inf.c_last; ++cb2)
-              pieces += slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
-            unsigned long long* cnt = a.counters + kPairCounterOffset +
-                                      static_cast<int64_t>(inf.seq) * hkv + inf.kvh;
-            if (static_cast<int>(tagged_increment(cnt, sm.gen)) == pieces && sm.n_merge < 2)
-              sm.merge_todo[sm.n_merge++] = inf;
-            __threadfence();
-          }
-          __syncwarp();
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&sm.mail_full));
       }
     }
-  }
-  __syncthreads();
-  // ---- merge the cut pairs whose last piece arrived here (log-sum-exp):
-  //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
-  if (!*reinterpret_cast<volatile int*>(&sm.abort_flag)) {
-    for (int j = 0; j < sm.n_merge; ++j) {
-      const StageInfo inf = sm.merge_todo[j];
+    // End marker for the merger.
+    if (mail_ok) {
+      const int k = posts++;
+      if (claim_mail(k)) {
+        if (warp == 0 && lane == 0) sm.mail_info.flags = kEnd;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.mail_full));
+      }
+    }
+  } else if (warp == kMergerWarp) {
+    // ------------------------------------------------------------ merger
+    // Takes the consumer warps' posts in order and combines their four
+    // states of the piece (log-sum-exp, as below).  A whole pair's output is
+    // written here; a cut piece's state goes to one of the block's two
+    // partial slots, is counted on the pair's arrival counter, and the post
+    // that brings the count to the pair's number of pieces merges all of
+    // them:
+    //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
+    int n_jobs = 0;  // merges handed to the merge warp
+    for (int k = 0;; ++k) {
+      const bool got = mbar_wait_sleepy(smem_u32(&sm.mail_full), k & 1, a.wait_limit_ns, 200);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) {
+          report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
+          atomicExch(&sm.abort_flag, 1);
+        }
+        break;
+      }
+      const StageInfo inf = sm.mail_info;
+      if (inf.flags & kEnd) break;
+      const bool bad = (inf.flags & kBad) != 0;
+      const bool single = (inf.flags & kSingle) != 0;
       const int64_t row_base = static_cast<int64_t>(inf.seq) * a.num_q_heads + inf.kvh * G;
-      for (int idx = threadIdx.x; idx < G * D; idx += kDecodeThreads) {
-        const int hh = idx / D;
-        const int d = idx - hh * D;
-        float M = -INFINITY;
-        bool bad = false;
-        for (int cb2 = inf.c_first; cb2 <= inf.c_last; ++cb2) {
-          if (slice_begin(cb2 + 1, T, nb) <= slice_begin(cb2, T, nb)) continue;
-          const int sl = cb2 == inf.c_first ? inf.first_slot : 0;
-          const int64_t r2 = (static_cast<int64_t>(cb2) * 2 + sl) * G + hh;
-          M = fmaxf(M, __ldcg(a.part_ml + r2 * 2));
-          bad |= __ldcg(a.part_ml + r2 * 2 + 1) < 0.f;
+      const int64_t prow = (static_cast<int64_t>(blockIdx.x) * 2 + inf.slot) * G;
+      // Per head: M = max over the four warps, weights 2^(m_w - M), L.
+      // Lane h (< G) computes head h's and the others read them by shuffle.
+      float hw[kConsumerWarps], hM = -INFINITY, hL = 0.f;
+      {
+        const int h = lane < G ? lane : 0;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) hM = fmaxf(hM, sm.mail_m[w][h]);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          hw[w] = hM == -INFINITY ? 0.f : fast_exp2(sm.mail_m[w][h] - hM);
+          hL += sm.mail_l[w][h] * hw[w];
         }
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-          for (int cb2 = inf.c_first; cb2 <= inf.c_last; ++cb2) {
-            if (slice_begin(cb2 + 1, T, nb) <= slice_begin(cb2, T, nb)) continue;
-            const int sl = cb2 == inf.c_first ? inf.first_slot : 0;
-            const int64_t r2 = (static_cast<int64_t>(cb2) * 2 + sl) * G + hh;
-            const float f = fast_exp2(__ldcg(a.part_ml + r2 * 2) - M);
-            L += __ldcg(a.part_ml + r2 * 2 + 1) * f;
-            O += __ldcg(a.part_o + r2 * D + d) * f;
+      }
+      // Each lane combines 4 consecutive dimensions per step (float4).
+      constexpr int kVec = G * D / 4;                   // float4 groups of the piece
+      constexpr int kPer = (kVec + 31) / 32;            // per lane
+      float4 res[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int v = lane + 32 * i;
+        const int hh = (v * 4) / D;
+        float wv[kConsumerWarps];
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) wv[w] = __shfl_sync(0xffffffffu, hw[w], hh & 31);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < kVec) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float4 x = reinterpret_cast<const float4*>(&sm.mail_o[w][0][0])[v];
+            acc.x += wv[w] * x.x;
+            acc.y += wv[w] * x.y;
+            acc.z += wv[w] * x.z;
+            acc.w += wv[w] * x.w;
           }
         }
-        const float r = (L > 0.f && !bad) ? O / L : 0.f;
-        static_cast<__nv_bfloat16*>(a.out)[(row_base + hh) * D + d] = __float2bfloat16_rn(r);
+        res[i] = acc;
+      }
+      // The mailbox has been read: let the consumers post again.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.mail_free));
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int v = lane + 32 * i;
+        const int hh = (v * 4) / D;
+        const float L = __shfl_sync(0xffffffffu, hL, hh & 31);
+        const float M = __shfl_sync(0xffffffffu, hM, hh & 31);
+        if (v >= kVec) continue;
+        const int d = v * 4 - hh * D;
+        if (single) {
+          const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+          uint2 packed;
+          packed.x = pack_bf16x2(res[i].x * inv, res[i].y * inv);
+          packed.y = pack_bf16x2(res[i].z * inv, res[i].w * inv);
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + (row_base + hh) * D + d) =
+              packed;
+        } else {
+          *reinterpret_cast<float4*>(a.part_o + (prow + hh) * D + d) = res[i];
+          if (d == 0) {
+            a.part_ml[(prow + hh) * 2 + 0] = M;
+            a.part_ml[(prow + hh) * 2 + 1] = bad ? -1.f : L;
+          }
+        }
+      }
+      if (single) continue;
+      __syncwarp();  // the partials of every lane precede lane 0's releasing add
+      int last = 0;
+      if (lane == 0) {
+        int pieces = 0;  // blocks with a non-empty slice in [c_first, c_last]
+        for (int cb2 = inf.c_first; cb2 <= inf.c_last; ++cb2)
+          pieces += slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
+        unsigned long long* cnt =
+            a.counters + kPairCounterOffset + static_cast<int64_t>(inf.seq) * hkv + inf.kvh;
+        last = static_cast<int>(tagged_increment(cnt, sm.gen)) == pieces;
+      }
+      if (__shfl_sync(0xffffffffu, last, 0) && n_jobs < 2) {
+        if (lane == 0) {
+          sm.job[n_jobs] = inf;
+          mbar_arrive(smem_u32(&sm.job_full[n_jobs]));
+        }
+        ++n_jobs;
       }
     }
-  }
-  __syncthreads();
-  // Count this block as finished; the last one advances the epoch, which
-  // gives the next launch a new generation.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (tagged_increment(a.counters + 1, sm.gen) == gridDim.x)
-      atomicExch(a.counters, sm.gen);  // epoch := generation (epoch + 1)
+    if (lane == 0) {  // end marker for the merge warp
+      sm.job[n_jobs].flags = kEnd;
+      mbar_arrive(smem_u32(&sm.job_full[n_jobs]));
+    }
+  } else if (warp == kMergeWarp) {
+    // ------------------------------------------------------------ merge warp
+    // Cut contexts whose last piece this block counted: merge all their
+    // pieces from the partial slots.  Off the consumers' path: the partial
+    // reads are L2 round trips, slow while the streams load the memory system.
+    for (int j = 0; j < 3; ++j) {
+      const bool got = mbar_wait_sleepy(smem_u32(&sm.job_full[j]), 0, a.wait_limit_ns, 500);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
+        break;
+      }
+      const StageInfo inf = sm.job[j];
+      if (inf.flags & kEnd) break;
+      fence_acq_rel_gpu();  // every lane: the other pieces' partials are visible
+      const int64_t row_base = static_cast<int64_t>(inf.seq) * a.num_q_heads + inf.kvh * G;
+      merge_pair<D, G>(a, inf, T, nb, row_base, lane);
+    }
   }
 }
 

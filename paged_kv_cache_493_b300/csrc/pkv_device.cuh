@@ -100,6 +100,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
+// The same wait for a warp whose wake-up is not urgent: it sleeps for
+// sleep_ns between tests, so that it takes few issue slots from the warps
+// that share its scheduler.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                 uint32_t sleep_ns) {
+  if (limit_ns == 0) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t start = global_timer_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - start > limit_ns) return false;
+  }
+}
+
 // Fixed bound used when draining copies already in flight before a block
 // exits after an expired wait (independent of the user-set limit).
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
