@@ -225,9 +225,9 @@ bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t nu
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
          encode_3d(&maps->v_rows, v, d, hkv, slots, s1, s2, 64, 1, kDecodeChunk,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_3d(&maps->k_sw128, k, d, hkv, slots, s1, s2, 64, 1, 128,
+         encode_3d(&maps->k_sw128, k, d, hkv, slots, s1, s2, 64, 1, kPrefillKeyTile,
                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode_3d(&maps->v_sw128, v, d, hkv, slots, s1, s2, 64, 1, 128,
+         encode_3d(&maps->v_sw128, v, d, hkv, slots, s1, s2, 64, 1, kPrefillKeyTile,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 

@@ -28,6 +28,7 @@ enum ErrSite : int {
   kSiteCombineContext = 220,
   kSitePrefillChunk = 300,
   kSitePrefillBlock = 301,
+  kSitePrefillAlign = 302,
   kSitePrefillWait = 310,  // + a small per-wait offset
 };
 
@@ -76,6 +77,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -310,6 +324,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_ma
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// Two non-negative finite floats to bf16 (round to nearest, ties away from
+// zero) with integer operations only: add half a bf16 ulp to the bit pattern
+// (a carry into the exponent is the correct rounding) and keep the upper
+// halves.  Keeps the conversion off the quarter-rate pipe that the
+// exponentials use.
+__device__ __forceinline__ uint32_t pack_bf16x2_nonneg(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

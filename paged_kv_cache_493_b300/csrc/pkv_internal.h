@@ -82,12 +82,14 @@ struct PrefillArgs {
 struct CacheMaps {
   CUtensorMap k_rows;   // decode: box {64, 1, 32} over [slots][Hkv][D], 128-byte swizzle
   CUtensorMap v_rows;
-  CUtensorMap k_sw128;  // prefill: box {64, 1, 128}, 128-byte swizzle
+  CUtensorMap k_sw128;  // prefill: box {64, 1, kPrefillKeyTile}, 128-byte swizzle
   CUtensorMap v_sw128;
 };
 
 // Decode chunk geometry (tokens per TMA transfer).
 constexpr int kDecodeChunk = 32;
+// Prefill key tile (keys per TMA transfer and per S tile).
+constexpr int kPrefillKeyTile = 64;
 
 cudaError_t launch_store_kvcache(const StoreArgs& a, cudaStream_t stream);
 

@@ -11,21 +11,26 @@
 //
 // One CTA computes a 128-row tile: 128/G consecutive queries x the G query
 // heads of one KV head, so every K/V tile is loaded once for the whole GQA
-// group.  Keys are visited in tiles of 128 (half a cache block), looked up
-// through the block table and loaded by TMA with 128-byte swizzle.
-//   warp 4     TMA producer (Q once, then K and V tiles, 2 stages each);
-//   warp 5     allocates 512 tensor-memory columns and issues the MMAs from
-//              one thread: S_j = Q K_j^T into one of two 128-column S buffers,
-//              then O += P_j V_j into the O columns (fp32 accumulators);
-//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r).  It reads
-//              S_j, applies scale and mask, keeps the running max m and sum
-//              l, writes P_j = exp2(S - m) as bf16 into shared memory in the
-//              layout the MMA reads, and rescales its O row in tensor memory
-//              when the max grew by more than 2^8 (the final division by l
-//              makes any reference value exact, so the rescale is deferred);
-//              finally O / l is written out as bf16.
-// MMA order S_0, S_1, PV_0, S_2, PV_1, ... lets S_{j+1} run while the softmax
-// works on S_j.
+// group.  Keys are visited in tiles of 64, looked up through the block table
+// and loaded by TMA with 128-byte swizzle.  Two CTAs share an SM (112 KB of
+// shared memory and 256 tensor-memory columns each): the softmax of one is
+// latency-bound, so a second independent pipeline fills its gaps.
+//   warp 4     TMA producer: Q once, then K tiles (2 stages);
+//   warp 6     TMA producer: V tiles (2 stages; K loads never queue behind a
+//              V stage that a PV still reads);
+//   warp 5     allocates 256 tensor-memory columns and issues the MMAs from
+//              one thread, as two streams each issued as soon as it is ready:
+//              S_j = Q K_j^T into one of two 64-column S buffers (needs K_j
+//              and the buffer back from the softmax of tile j - 2, which
+//              releases it as soon as it has loaded it), and O += P_j V_j
+//              into the O columns (needs P_j and V_j), fp32 accumulators;
+//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r).  It loads
+//              S_j, releases its buffer, applies scale and mask, keeps the
+//              running max m and sum l, writes P_j = exp2(S - m) as bf16 into
+//              shared memory in the layout the MMA reads, and rescales its O
+//              row in tensor memory when the max grew by more than 2^8 (the
+//              final division by l makes any reference value exact, so the
+//              rescale is deferred); finally O / l is written out as bf16.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -33,51 +38,57 @@ namespace pkv {
 
 namespace {
 
-constexpr int kRows = 128;      // MMA M: query rows per tile
-constexpr int kKeyTile = 128;   // keys per tile (MMA N of QK^T, K of PV)
+constexpr int kRows = 128;        // MMA M: query rows per tile
+constexpr int kKeyTile = kPrefillKeyTile;  // keys per tile (MMA N of QK^T, K of PV)
 constexpr int kKvStages = 2;
-constexpr int kPrefillThreads = 192;
-constexpr int kTmemCols = 512;
-constexpr int kSCol0 = 0;       // S buffers at columns 0 and 128
-constexpr int kOCol = 256;      // O at columns 256 .. 256 + D
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;  // Q and K tiles
+constexpr int kMmaWarp = 5;
+constexpr int kVProducerWarp = 6;
+constexpr int kPrefillThreads = 7 * 32;
+constexpr int kCtasPerSm = 2;
+constexpr int kTmemCols = 256;
+constexpr int kSCol0 = 0;         // S buffers at columns 0 and kKeyTile
+constexpr int kOCol = 2 * kKeyTile;  // O at columns kOCol .. kOCol + D
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct PrefillLayout {
   static constexpr int kPanels = D / 64;                 // 64-element (128-byte) column panels
-  static constexpr int kPanelBytes = kRows * 128;        // 128 rows x 128 bytes
+  static constexpr int kQPanel = kRows * 128;            // 128 query rows x 128 bytes
+  static constexpr int kKvPanel = kKeyTile * 128;        // 64 key rows x 128 bytes
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kPanels * kPanelBytes;  // stages of K
-  static constexpr int kV = kK + kKvStages * kPanels * kPanelBytes;
-  static constexpr int kP = kV + kKvStages * kPanels * kPanelBytes;
-  static constexpr int kBar = kP + 2 * kPanelBytes;      // P: 128 keys = 2 panels
+  static constexpr int kK = kQ + kPanels * kQPanel;      // stages of K
+  static constexpr int kV = kK + kKvStages * kPanels * kKvPanel;
+  static constexpr int kP = kV + kKvStages * kPanels * kKvPanel;
+  static constexpr int kPBytes = kRows * kKeyTile * 2;   // P: 128 rows x 64 keys = one panel
+  static constexpr int kBar = kP + kPBytes;
   // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  //           p_full, o_done, drain   (15 x 8 bytes) + misc words
-  static constexpr int kMisc = kBar + 16 * 8;
+  //           s_free[2], p_full, pv_done[2], drain   (17 x 8 bytes) + misc words
+  static constexpr int kMisc = kBar + 24 * 8;
   static constexpr int kBytes = kMisc + 64;
-  static constexpr int kAlloc = kBytes + 1024;           // slack for 1024-byte alignment
+  static_assert(kKeyTile * 2 == 128, "P is one 128-byte-swizzled panel");
 };
 
 struct PrefillBars {
-  uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, o_done, drain;
+  uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full,
+      pv_done[2], drain;
 };
 
 __device__ __forceinline__ PrefillBars make_bars(uint32_t base) {
   PrefillBars b;
   b.q_full = base;
-  b.k_full[0] = base + 8;
-  b.k_full[1] = base + 16;
-  b.k_empty[0] = base + 24;
-  b.k_empty[1] = base + 32;
-  b.v_full[0] = base + 40;
-  b.v_full[1] = base + 48;
-  b.v_empty[0] = base + 56;
-  b.v_empty[1] = base + 64;
-  b.s_full[0] = base + 72;
-  b.s_full[1] = base + 80;
-  b.p_full = base + 88;
-  b.o_done = base + 96;
-  b.drain = base + 104;
+  for (int s = 0; s < 2; ++s) {
+    b.k_full[s] = base + 8 + 8 * s;
+    b.k_empty[s] = base + 24 + 8 * s;
+    b.v_full[s] = base + 40 + 8 * s;
+    b.v_empty[s] = base + 56 + 8 * s;
+    b.s_full[s] = base + 72 + 8 * s;
+    b.s_free[s] = base + 88 + 8 * s;
+    b.pv_done[s] = base + 112 + 8 * s;
+  }
+  b.p_full = base + 104;
+  b.drain = base + 128;
   return b;
 }
 
@@ -113,7 +124,7 @@ __device__ __forceinline__ TileInfo find_tile(const PrefillArgs& a, int t, int q
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(kPrefillThreads, kCtasPerSm)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, PrefillArgs a) {
   using L = PrefillLayout<D>;
@@ -121,9 +132,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   constexpr uint32_t kKTileBytes = kKeyTile * D * 2;
   constexpr uint32_t kQBytes = kRows * D * 2;
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint8_t* sgen = smem_raw + (sbase - smem_u32(smem_raw));
+  // The 128-byte swizzle repeats every 1024 bytes: the panels need a
+  // 1024-byte-aligned base.  Dynamic shared memory starts there (no static
+  // shared memory in this kernel); a misaligned base is reported, not used.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t sbase = smem_u32(smem_raw);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) report_error(a.err, kErrDeviceCheck, kSitePrefillAlign);
+    return;
+  }
+  uint8_t* sgen = smem_raw;
   const PrefillBars bar = make_bars(sbase + L::kBar);
   volatile int* misc = reinterpret_cast<volatile int*>(sgen + L::kMisc);
   // misc[0] tmem base, misc[1] abort flag, misc[2] bad tile
@@ -141,20 +159,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(bar.v_full[s], 1);
       mbar_init(bar.v_empty[s], 1);
       mbar_init(bar.s_full[s], 1);
+      mbar_init(bar.s_free[s], kSoftmaxWarps);
+      mbar_init(bar.pv_done[s], 1);
     }
-    mbar_init(bar.p_full, kRows);
-    mbar_init(bar.o_done, 1);
+    mbar_init(bar.p_full, kSoftmaxWarps * 32);
     mbar_init(bar.drain, 1);
     misc[1] = 0;
     misc[2] = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&qmap);
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(sbase + L::kMisc, kTmemCols);
     tmem_relinquish();
   }
@@ -175,7 +194,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
   }
   const int32_t* table = a.block_tables + static_cast<int64_t>(max(ti.seq, 0)) * a.max_blocks;
-  if (warp == 4 && ti.valid && !bad) {
+  if (warp == kProducerWarp && ti.valid && !bad) {
     const int nblk = (nkt * kKeyTile + kBlockSize - 1) / kBlockSize;
     bool b = false;
     for (int i = lane; i < nblk; i += 32) {
@@ -192,14 +211,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     report_error(a.err, kErrDeviceCheck, bad ? kSitePrefillChunk : kSitePrefillBlock);
   const bool run = ti.valid && !bad && misc[2] == 0 && nkt > 0;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer (Q, K)
     if (lane == 0 && run) {
-      int k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+      int k_last[2] = {-1, -1};
       mbar_arrive_expect_tx(bar.q_full, kQBytes);
 #pragma unroll
       for (int p = 0; p < L::kPanels; ++p)
-        tma_load_3d(sbase + L::kQ + p * L::kPanelBytes, &qmap, bar.q_full, p * 64, kvh * G,
+        tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full, p * 64, kvh * G,
                     ti.q_row0 + ti.qt_start);
       for (int j = 0; j < nkt; ++j) {
         const int st = j & 1;
@@ -215,9 +234,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_arrive_expect_tx(bar.k_full[st], kKTileBytes);
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sbase + L::kK + (st * L::kPanels + p) * L::kPanelBytes, &kmap,
-                      bar.k_full[st], p * 64, kvh, slot);
+          tma_load_3d(sbase + L::kK + (st * L::kPanels + p) * L::kKvPanel, &kmap, bar.k_full[st],
+                      p * 64, kvh, slot);
         k_last[st] = j;
+      }
+      // Every copy issued must land before the block may exit, whether or
+      // not its consumer gave up on it (after a normal run these waits
+      // return at once).
+      mbar_wait(bar.q_full, 0, kDrainLimitNs);
+      for (int s = 0; s < 2; ++s)
+        if (k_last[s] >= 0) mbar_wait(bar.k_full[s], (k_last[s] >> 1) & 1, kDrainLimitNs);
+    }
+  } else if (warp == kVProducerWarp) {
+    // ------------------------------------------------------------ producer (V)
+    if (lane == 0 && run) {
+      int v_last[2] = {-1, -1};
+      for (int j = 0; j < nkt; ++j) {
+        const int st = j & 1;
+        const int k0 = j * kKeyTile;
+        const int slot = table[k0 / kBlockSize] * kBlockSize + (k0 % kBlockSize);
         if (j >= kKvStages &&
             !mbar_wait(bar.v_empty[st], ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
           report_error(a.err, kErrTimeout, kSitePrefillWait + 1);
@@ -228,77 +263,77 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_arrive_expect_tx(bar.v_full[st], kKTileBytes);
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sbase + L::kV + (st * L::kPanels + p) * L::kPanelBytes, &vmap,
-                      bar.v_full[st], p * 64, kvh, slot);
+          tma_load_3d(sbase + L::kV + (st * L::kPanels + p) * L::kKvPanel, &vmap, bar.v_full[st],
+                      p * 64, kvh, slot);
         v_last[st] = j;
       }
-      // Every copy issued must land before the block may exit, whether or
-      // not its consumer gave up on it (after a normal run these waits
-      // return at once).
-      mbar_wait(bar.q_full, 0, kDrainLimitNs);
-      for (int s = 0; s < 2; ++s) {
-        if (k_last[s] >= 0) mbar_wait(bar.k_full[s], (k_last[s] >> 1) & 1, kDrainLimitNs);
+      for (int s = 0; s < 2; ++s)
         if (v_last[s] >= 0) mbar_wait(bar.v_full[s], (v_last[s] >> 1) & 1, kDrainLimitNs);
-      }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && run) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeyTile, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, true);
       bool ok = mbar_wait(bar.q_full, 0, a.wait_limit_ns);
       if (!ok) report_error(a.err, kErrTimeout, kSitePrefillWait + 2);
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {  // S_j = Q K_j^T
-          const int st = j & 1;
-          if (!mbar_wait(bar.k_full[st], (j >> 1) & 1, a.wait_limit_ns)) {
-            report_error(a.err, kErrTimeout, kSitePrefillWait + 3);
-            ok = false;
-            break;
-          }
-          if (misc[1]) {
-            ok = false;
-            break;
-          }
+      int js = 0, jp = 0;
+      bool idle = false;
+      uint64_t idle_since = 0;
+      while (ok && jp < nkt) {
+        bool did = false;
+        if (js < nkt && (js < 2 || mbar_test(bar.s_free[js & 1], ((js - 2) >> 1) & 1)) &&
+            mbar_test(bar.k_full[js & 1], (js >> 1) & 1)) {  // S_js = Q K_js^T
+          const int st = js & 1;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kSCol0 + st * kKeyTile;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            const uint64_t ad = smem_desc_sw128(sbase + L::kQ + off, 16, 1024);
+            const uint32_t qoff = (kk >> 2) * L::kQPanel + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * L::kKvPanel + (kk & 3) * 32;
+            const uint64_t ad = smem_desc_sw128(sbase + L::kQ + qoff, 16, 1024);
             const uint64_t bd =
-                smem_desc_sw128(sbase + L::kK + st * L::kPanels * L::kPanelBytes + off, 16, 1024);
+                smem_desc_sw128(sbase + L::kK + st * L::kPanels * L::kKvPanel + koff, 16, 1024);
             tc_mma_ss(d_tmem, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
           }
           tc_commit(bar.s_full[st]);
           tc_commit(bar.k_empty[st]);
+          ++js;
+          did = true;
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int jj = j - 1;
-          const int st = jj & 1;
-          if (!mbar_wait(bar.p_full, jj & 1, a.wait_limit_ns) ||
-              !mbar_wait(bar.v_full[st], (jj >> 1) & 1, a.wait_limit_ns)) {
-            report_error(a.err, kErrTimeout, kSitePrefillWait + 4);
-            ok = false;
-            break;
-          }
-          if (misc[1]) {
-            ok = false;
-            break;
-          }
+        if (jp < js && mbar_test(bar.p_full, jp & 1) &&
+            mbar_test(bar.v_full[jp & 1], (jp >> 1) & 1)) {  // O += P_jp V_jp
+          const int st = jp & 1;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-            const uint32_t a_off = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            const uint64_t ad = smem_desc_sw128(sbase + L::kP + a_off, 16, 1024);
-            // V stage: [128 keys][64 d] panels; 16 keys = 2 x 8-row groups.
+            const uint64_t ad = smem_desc_sw128(sbase + L::kP + kk * 32, 16, 1024);
+            // V stage: [64 keys][64 d] panels; 16 keys = 2 x 8-row groups.
             const uint64_t bd = smem_desc_sw128(
-                sbase + L::kV + st * L::kPanels * L::kPanelBytes + kk * 16 * 128,
-                L::kPanelBytes, 1024);
-            tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+                sbase + L::kV + st * L::kPanels * L::kKvPanel + kk * 16 * 128, L::kKvPanel, 1024);
+            tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar.o_done);
+          tc_commit(bar.pv_done[st]);
           tc_commit(bar.v_empty[st]);
+          ++jp;
+          did = true;
+        }
+        if (did) {
+          idle = false;
+          continue;
+        }
+        if (misc[1]) {
+          ok = false;
+          break;
+        }
+        const uint64_t now = global_timer_ns();
+        if (!idle) {
+          idle = true;
+          idle_since = now;
+        } else if (now - idle_since > a.wait_limit_ns) {
+          report_error(a.err, kErrTimeout, kSitePrefillWait + 3);
+          ok = false;
+          break;
         }
       }
       if (!ok) misc[1] = 1;
@@ -316,9 +351,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const bool row_real = run && qi < ti.lq;
     const int lim = run ? min(ti.ctx - ti.lq + qi, ti.ctx - 1) : 0;  // last visible key
     const int pos_min = run ? ti.ctx - ti.lq + ti.qt_start : 0;       // smallest row position
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // reference max (log2 domain, may lag by < 2^8) and sum
     bool ok = run;
-    uint8_t* prow = sgen + L::kP + r * 128;
+    // A masked raw score: it must vanish in the max (or min, for a negative
+    // scale) and give exp2(-inf) = 0.
+    const float masked = sl2 >= 0.f ? -INFINITY : INFINITY;
+    const uint32_t prow = sbase + L::kP + r * 128;
     for (int j = 0; ok && j < nkt; ++j) {
       // Exit decisions are warp-uniform: tcgen05.ld/st are warp-collective.
       const bool got = mbar_wait(bar.s_full[j & 1], (j >> 1) & 1, a.wait_limit_ns);
@@ -338,33 +376,51 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tmem_ld_32x32b_x32(trow + kSCol0 + (j & 1) * kKeyTile + c * 32,
                            *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_wait_ld();
-      const int k0 = j * kKeyTile;
-      const bool need_mask = (k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx);
-      float mt = -INFINITY;
-      if (need_mask) {
+      // S_j is in registers: its tensor-memory buffer may take S_{j+2}.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.s_free[j & 1]);
+      const int k0 = j * kKeyTile;  // key of x[0]
+      if ((k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx)) {
 #pragma unroll
-        for (int c = 0; c < kKeyTile; ++c) {
-          x[c] = (k0 + c <= lim) ? x[c] * sl2 : -INFINITY;
-          mt = fmaxf(mt, x[c]);
-        }
+        for (int c = 0; c < kKeyTile; ++c)
+          if (k0 + c > lim) x[c] = masked;
+      }
+      // Row max of the scaled scores, from 8 independent partial maxima of
+      // the raw ones (the scale's sign decides max or min).
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = x[i];
+      if (sl2 >= 0.f) {
+#pragma unroll
+        for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+#pragma unroll
+        for (int i = 4; i > 0; i >>= 1)
+#pragma unroll
+          for (int k = 0; k < i; ++k) mp[k] = fmaxf(mp[k], mp[k + i]);
       } else {
 #pragma unroll
-        for (int c = 0; c < kKeyTile; ++c) {
-          x[c] *= sl2;
-          mt = fmaxf(mt, x[c]);
+        for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fminf(mp[c & 7], x[c]);
+#pragma unroll
+        for (int i = 4; i > 0; i >>= 1)
+#pragma unroll
+          for (int k = 0; k < i; ++k) mp[k] = fminf(mp[k], mp[k + i]);
+      }
+      const float m_new = fmaxf(m, mp[0] * sl2);
+      const bool need = m_new > m + kRescaleThreshold;  // true on the first tile
+      // O and the P buffer were last used by PV of tile j - 1.
+      if (j >= 1) {
+        const bool got_o =
+            mbar_wait(bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, got_o)) {
+          if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 6);
+          ok = false;
+          break;
         }
       }
-      const float m_new = fmaxf(m, mt);
-      const bool got_o = (j == 0) || mbar_wait(bar.o_done, (j - 1) & 1, a.wait_limit_ns);
-      if (!__all_sync(0xffffffffu, got_o)) {
-        if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 6);
-        ok = false;
-        break;
-      }
-      const bool need = m_new > m + kRescaleThreshold;  // true on the first tile
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? fast_exp2(m - m_new) : 1.f;
-        if (j > 0) {
+        if (j >= 1) {
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -382,34 +438,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           m = m_new;
         }
       }
-      // P = exp2(x - m) -> bf16, row r of two 128-byte-swizzled panels
-      float rs = 0.f;
+      // P = exp2(scale * x - m) -> bf16, row r of the 128-byte-swizzled panel
+      // (every key of the row masked so far: m = -inf, P = 0)
+      const float neg_m = m == -INFINITY ? 0.f : -m;
+      float rs[8];
 #pragma unroll
-      for (int pnl = 0; pnl < 2; ++pnl) {
+      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t w[4];
+      for (int ch = 0; ch < kKeyTile / 8; ++ch) {
+        uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(x[pnl * 64 + ch * 8 + 2 * e] - m);
-            const float p1 = fast_exp2(x[pnl * 64 + ch * 8 + 2 * e + 1] - m);
-            rs += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
-          }
-          const uint32_t addr = smem_u32(prow) + pnl * L::kPanelBytes + ((ch ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(fmaf(x[ch * 8 + 2 * e], sl2, neg_m));
+          const float p1 = fast_exp2(fmaf(x[ch * 8 + 2 * e + 1], sl2, neg_m));
+          rs[e] += p0;
+          rs[e + 4] += p1;
+          w[e] = pack_bf16x2_nonneg(p0, p1);
         }
+        const uint32_t addr = prow + ((ch ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
       }
-      l += rs;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar.p_full);
     }
     // ---- epilogue: O / l -> bf16
     if (ok && nkt > 0) {  // ok is warp-uniform here
-      const bool got = mbar_wait(bar.o_done, (nkt - 1) & 1, a.wait_limit_ns);
+      const bool got =
+          mbar_wait(bar.pv_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 7);
         ok = false;
@@ -450,7 +509,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -462,7 +521,11 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
   using L = PrefillLayout<D>;
   auto kern = prefill_kernel<D, G>;
   cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  // Two CTAs per SM need the largest shared-memory carve-out.
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   constexpr int QT = kRows / G;
   // Upper bound on the number of tiles: sum_s ceil(Lq_s / QT) <= total/QT + num_seqs.
@@ -476,7 +539,7 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kPrefillThreads);
-  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
