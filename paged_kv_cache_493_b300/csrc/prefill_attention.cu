@@ -12,7 +12,7 @@
 // One CTA computes a 128-row tile: 128/G consecutive queries x the G query
 // heads of one KV head, so every K/V tile is loaded once for the whole GQA
 // group.  Keys are visited in tiles of 64, looked up through the block table
-// and loaded by TMA with 128-byte swizzle.  Two CTAs share an SM (112 KB of
+// and loaded by TMA with 128-byte swizzle.  Two CTAs share an SM (96 KB of
 // shared memory and 256 tensor-memory columns each): the softmax of one is
 // latency-bound, so a second independent pipeline fills its gaps.
 //   warp 4     TMA producer: Q once, then K tiles (2 stages);
@@ -20,17 +20,18 @@
 //              V stage that a PV still reads);
 //   warp 5     allocates 256 tensor-memory columns and issues the MMAs from
 //              one thread, as two streams each issued as soon as it is ready:
-//              S_j = Q K_j^T into one of two 64-column S buffers (needs K_j
-//              and the buffer back from the softmax of tile j - 2, which
-//              releases it as soon as it has loaded it), and O += P_j V_j
-//              into the O columns (needs P_j and V_j), fp32 accumulators;
+//              S_j = Q K_j^T into one of two 64-column S buffers (needs K_j,
+//              and PV_{j-2} issued: P_{j-2} sits in that buffer and the tensor
+//              pipe executes in order), and O += P_j V_j with P_j read from
+//              tensor memory (needs P_j and V_j), fp32 accumulators;
 //   warps 0-3  softmax: thread r owns row r (tensor-memory lane r).  It loads
-//              S_j, releases its buffer, applies scale and mask, keeps the
-//              running max m and sum l, writes P_j = exp2(S - m) as bf16 into
-//              shared memory in the layout the MMA reads, and rescales its O
-//              row in tensor memory when the max grew by more than 2^8 (the
-//              final division by l makes any reference value exact, so the
-//              rescale is deferred); finally O / l is written out as bf16.
+//              S_j, applies scale and mask, keeps the running max m and sum
+//              l, writes P_j = exp2(S - m) as bf16 pairs over the first half
+//              of S_j's own columns (so P is double-buffered with S, and no
+//              shared memory is used for it), and rescales its O row in
+//              tensor memory when the max grew by more than 2^8 (the final
+//              division by l makes any reference value exact, so the rescale
+//              is deferred); finally O / l is written out as bf16.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -60,18 +61,15 @@ struct PrefillLayout {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kPanels * kQPanel;      // stages of K
   static constexpr int kV = kK + kKvStages * kPanels * kKvPanel;
-  static constexpr int kP = kV + kKvStages * kPanels * kKvPanel;
-  static constexpr int kPBytes = kRows * kKeyTile * 2;   // P: 128 rows x 64 keys = one panel
-  static constexpr int kBar = kP + kPBytes;
+  static constexpr int kBar = kV + kKvStages * kPanels * kKvPanel;
   // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-  //           s_free[2], p_full, pv_done[2], drain   (17 x 8 bytes) + misc words
+  //           p_full[2], pv_done[2], drain   (17 x 8 bytes) + misc words
   static constexpr int kMisc = kBar + 24 * 8;
   static constexpr int kBytes = kMisc + 64;
-  static_assert(kKeyTile * 2 == 128, "P is one 128-byte-swizzled panel");
 };
 
 struct PrefillBars {
-  uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_free[2], p_full,
+  uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
       pv_done[2], drain;
 };
 
@@ -84,11 +82,10 @@ __device__ __forceinline__ PrefillBars make_bars(uint32_t base) {
     b.v_full[s] = base + 40 + 8 * s;
     b.v_empty[s] = base + 56 + 8 * s;
     b.s_full[s] = base + 72 + 8 * s;
-    b.s_free[s] = base + 88 + 8 * s;
-    b.pv_done[s] = base + 112 + 8 * s;
+    b.p_full[s] = base + 88 + 8 * s;
+    b.pv_done[s] = base + 104 + 8 * s;
   }
-  b.p_full = base + 104;
-  b.drain = base + 128;
+  b.drain = base + 120;
   return b;
 }
 
@@ -159,10 +156,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(bar.v_full[s], 1);
       mbar_init(bar.v_empty[s], 1);
       mbar_init(bar.s_full[s], 1);
-      mbar_init(bar.s_free[s], kSoftmaxWarps);
+      mbar_init(bar.p_full[s], kSoftmaxWarps * 32);
       mbar_init(bar.pv_done[s], 1);
     }
-    mbar_init(bar.p_full, kSoftmaxWarps * 32);
     mbar_init(bar.drain, 1);
     misc[1] = 0;
     misc[2] = 0;
@@ -282,8 +278,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       uint64_t idle_since = 0;
       while (ok && jp < nkt) {
         bool did = false;
-        if (js < nkt && (js < 2 || mbar_test(bar.s_free[js & 1], ((js - 2) >> 1) & 1)) &&
-            mbar_test(bar.k_full[js & 1], (js >> 1) & 1)) {  // S_js = Q K_js^T
+        // S_js overwrites the columns where P_{js-2} sits: only after PV_{js-2}
+        // has been issued (the tensor pipe executes in order).
+        if (js < nkt && js - 2 < jp && mbar_test(bar.k_full[js & 1], (js >> 1) & 1)) {  // S_js = Q K_js^T
           const int st = js & 1;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kSCol0 + st * kKeyTile;
@@ -301,17 +298,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           ++js;
           did = true;
         }
-        if (jp < js && mbar_test(bar.p_full, jp & 1) &&
+        if (jp < js && mbar_test(bar.p_full[jp & 1], (jp >> 1) & 1) &&
             mbar_test(bar.v_full[jp & 1], (jp >> 1) & 1)) {  // O += P_jp V_jp
           const int st = jp & 1;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kKeyTile / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sbase + L::kP + kk * 32, 16, 1024);
+            // P_jp: bf16 pairs in the first kKeyTile / 2 columns of S buffer st.
+            const uint32_t a_tmem = tmem + kSCol0 + st * kKeyTile + kk * 8;
             // V stage: [64 keys][64 d] panels; 16 keys = 2 x 8-row groups.
             const uint64_t bd = smem_desc_sw128(
                 sbase + L::kV + st * L::kPanels * L::kKvPanel + kk * 16 * 128, L::kKvPanel, 1024);
-            tc_mma_ss(tmem + kOCol, ad, bd, idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + kOCol, a_tmem, bd, idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar.pv_done[st]);
           tc_commit(bar.v_empty[st]);
@@ -335,6 +333,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           ok = false;
           break;
         }
+        __nanosleep(32);  // leave the scheduler's issue slots to the softmax warps
       }
       if (!ok) misc[1] = 1;
       // Every MMA issued must finish before tensor memory is released.
@@ -356,7 +355,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // A masked raw score: it must vanish in the max (or min, for a negative
     // scale) and give exp2(-inf) = 0.
     const float masked = sl2 >= 0.f ? -INFINITY : INFINITY;
-    const uint32_t prow = sbase + L::kP + r * 128;
     for (int j = 0; ok && j < nkt; ++j) {
       // Exit decisions are warp-uniform: tcgen05.ld/st are warp-collective.
       const bool got = mbar_wait(bar.s_full[j & 1], (j >> 1) & 1, a.wait_limit_ns);
@@ -376,10 +374,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tmem_ld_32x32b_x32(trow + kSCol0 + (j & 1) * kKeyTile + c * 32,
                            *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_wait_ld();
-      // S_j is in registers: its tensor-memory buffer may take S_{j+2}.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.s_free[j & 1]);
       const int k0 = j * kKeyTile;  // key of x[0]
       if ((k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx)) {
 #pragma unroll
@@ -408,19 +402,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
       const float m_new = fmaxf(m, mp[0] * sl2);
       const bool need = m_new > m + kRescaleThreshold;  // true on the first tile
-      // O and the P buffer were last used by PV of tile j - 1.
-      if (j >= 1) {
-        const bool got_o =
-            mbar_wait(bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, got_o)) {
-          if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 6);
-          ok = false;
-          break;
-        }
-      }
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? fast_exp2(m - m_new) : 1.f;
         if (j >= 1) {
+          // O holds PV up to tile j - 1: wait for it before rescaling.
+          const bool got_o =
+              mbar_wait(bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.wait_limit_ns);
+          if (!__all_sync(0xffffffffu, got_o)) {
+            if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 6);
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -438,32 +430,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           m = m_new;
         }
       }
-      // P = exp2(scale * x - m) -> bf16, row r of the 128-byte-swizzled panel
-      // (every key of the row masked so far: m = -inf, P = 0)
+      // P = exp2(scale * x - m) -> bf16 pairs over the first half of S_j's
+      // columns, where the PV MMA reads them (every key of the row masked so
+      // far: m = -inf, P = 0)
       const float neg_m = m == -INFINITY ? 0.f : -m;
       float rs[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      uint32_t pw[kKeyTile / 2];
 #pragma unroll
-      for (int ch = 0; ch < kKeyTile / 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(fmaf(x[ch * 8 + 2 * e], sl2, neg_m));
-          const float p1 = fast_exp2(fmaf(x[ch * 8 + 2 * e + 1], sl2, neg_m));
-          rs[e] += p0;
-          rs[e + 4] += p1;
-          w[e] = pack_bf16x2_nonneg(p0, p1);
-        }
-        const uint32_t addr = prow + ((ch ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
-                     "r"(w[1]), "r"(w[2]), "r"(w[3])
-                     : "memory");
+      for (int c = 0; c < kKeyTile / 2; ++c) {
+        const float p0 = fast_exp2(fmaf(x[2 * c], sl2, neg_m));
+        const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, neg_m));
+        rs[c & 3] += p0;
+        rs[(c & 3) + 4] += p1;
+        pw[c] = pack_bf16x2_nonneg(p0, p1);
       }
+      static_assert(kKeyTile / 2 == 32, "one 32-column store per row");
+      tmem_st_32x32b_x32(trow + kSCol0 + (j & 1) * kKeyTile, pw);
+      tmem_wait_st();
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar.p_full);
+      mbar_arrive(bar.p_full[j & 1]);
     }
     // ---- epilogue: O / l -> bf16
     if (ok && nkt > 0) {  // ok is warp-uniform here
