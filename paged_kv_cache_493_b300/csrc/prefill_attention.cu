@@ -381,24 +381,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           if (k0 + c > lim) x[c] = masked;
       }
       // Row max of the scaled scores, from 8 independent partial maxima of
-      // the raw ones (the scale's sign decides max or min).
+      // the raw ones (three-input max; the scale's sign decides max or min).
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = x[i];
       if (sl2 >= 0.f) {
 #pragma unroll
-        for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-#pragma unroll
-        for (int i = 4; i > 0; i >>= 1)
-#pragma unroll
-          for (int k = 0; k < i; ++k) mp[k] = fmaxf(mp[k], mp[k + i]);
+        for (int c = 8; c < kKeyTile; c += 2) mp[(c >> 1) & 7] = fmax3(mp[(c >> 1) & 7], x[c], x[c + 1]);
+        mp[0] = fmax3(mp[0], mp[1], mp[2]);
+        mp[3] = fmax3(mp[3], mp[4], mp[5]);
+        mp[0] = fmax3(mp[0], mp[3], fmaxf(mp[6], mp[7]));
       } else {
 #pragma unroll
-        for (int c = 8; c < kKeyTile; ++c) mp[c & 7] = fminf(mp[c & 7], x[c]);
-#pragma unroll
-        for (int i = 4; i > 0; i >>= 1)
-#pragma unroll
-          for (int k = 0; k < i; ++k) mp[k] = fminf(mp[k], mp[k + i]);
+        for (int c = 8; c < kKeyTile; c += 2) mp[(c >> 1) & 7] = fmin3(mp[(c >> 1) & 7], x[c], x[c + 1]);
+        mp[0] = fmin3(mp[0], mp[1], mp[2]);
+        mp[3] = fmin3(mp[3], mp[4], mp[5]);
+        mp[0] = fmin3(mp[0], mp[3], fminf(mp[6], mp[7]));
       }
       const float m_new = fmaxf(m, mp[0] * sl2);
       const bool need = m_new > m + kRescaleThreshold;  // true on the first tile
@@ -434,21 +432,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       // columns, where the PV MMA reads them (every key of the row masked so
       // far: m = -inf, P = 0)
       const float neg_m = m == -INFINITY ? 0.f : -m;
-      float rs[8];
+      // Pairs of keys in packed two-wide fp32 (scale-and-shift, row sum).
+      const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
+      uint64_t rs2[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      for (int i = 0; i < 4; ++i) rs2[i] = 0ull;
       uint32_t pw[kKeyTile / 2];
 #pragma unroll
       for (int c = 0; c < kKeyTile / 2; ++c) {
-        const float p0 = fast_exp2(fmaf(x[2 * c], sl2, neg_m));
-        const float p1 = fast_exp2(fmaf(x[2 * c + 1], sl2, neg_m));
-        rs[c & 3] += p0;
-        rs[(c & 3) + 4] += p1;
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), sc2, nm2), y0, y1);
+        const float p0 = fast_exp2(y0);
+        const float p1 = fast_exp2(y1);
+        rs2[c & 3] = f2_add(rs2[c & 3], f2_pack(p0, p1));
         pw[c] = pack_bf16x2_nonneg(p0, p1);
       }
       static_assert(kKeyTile / 2 == 32, "one 32-column store per row");
       tmem_st_32x32b_x32(trow + kSCol0 + (j & 1) * kKeyTile, pw);
       tmem_wait_st();
+      float rs[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) f2_unpack(rs2[i], rs[i], rs[i + 4]);
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tc_fence_before();
       mbar_arrive(bar.p_full[j & 1]);
