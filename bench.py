@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # from the ncu capture summarised in profiles/decode_split_qwen_decode_b128.md.
 # Valid only for the kernel version that capture measured: set to None when
 # the kernel changes, until it is captured again.
-DECODE_SPLIT_TRAFFIC_BYTES = 328.7e6
+DECODE_SPLIT_TRAFFIC_BYTES = 328.3e6
 
 
 # ----------------------------------------------------------------------------- ranks
