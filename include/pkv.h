@@ -13,8 +13,8 @@
  *
  *   pkv_store_kvcache      scatter of new K/V rows into cache slots;
  *   pkv_decode_attention   one query token per sequence over its cache
- *                          (split-K over the context, then a log-sum-exp
- *                          combine);
+ *                          (contexts split across blocks, pieces merged
+ *                          by log-sum-exp inside the same kernel);
  *   pkv_prefill_attention  a chunk of query tokens per sequence over its
  *                          cached prefix plus the chunk itself, causal.
  *
@@ -111,19 +111,19 @@ pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
  *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K[s][t][g(h)]) * V[s][t][g(h)]
  *
  * with fp32 accumulation and bf16 (round to nearest even) output.  A
- * sequence with context 0 gets a zero output.  The context is split into
- * ranges processed in parallel (flash decoding; the number of ranges per
- * sequence is chosen from the batch shape and capped by pkv_set_max_splits)
- * and the partial results are merged by a log-sum-exp combine.  The
- * sequences' contexts, laid end to end, are cut into equal slices, one per
- * block of a grid that fills the GPU once (stream-K), so long and short
- * contexts balance; only a context cut by a slice boundary is merged, by
- * the block that finishes its last piece (one kernel launch in all).  The
- * per-pair arrival counters and the partials live in a library-owned workspace
- * on the current device, allocated (and grown) with cudaMalloc on first
- * need; call pkv_reserve_workspace before capturing this call in a CUDA
- * graph.  Calls on different streams that overlap share that workspace and
- * must be serialised by the caller.
+ * sequence with context 0 gets a zero output.  Contexts are split and
+ * processed in parallel (flash decoding): the (sequence, KV head) contexts
+ * of the batch, laid end to end, are cut into equal slices, one per block
+ * of a grid that fills the GPU once (stream-K), so long and short contexts
+ * balance; a context cut by a slice boundary has its pieces merged by
+ * log-sum-exp by the block that finishes its last piece (one kernel launch
+ * in all).  pkv_set_max_splits caps the grid.  The per-context arrival
+ * counters and the partials live in a library-owned workspace on the
+ * current device, allocated (and grown) with cudaMalloc on first need; call
+ * pkv_reserve_workspace before capturing this call in a CUDA graph (replays
+ * of the captured call are then correct: the counters carry a launch
+ * generation kept on the device).  Calls on different streams that overlap
+ * share that workspace and must be serialised by the caller.
  */
 pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
                                 const void* v_cache, int64_t num_blocks,

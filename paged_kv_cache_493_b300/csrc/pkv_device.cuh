@@ -25,7 +25,6 @@ enum ErrSite : int {
   kSiteDecodeWaitFull = 210,
   kSiteDecodeWaitEmpty = 211,
   kSiteDecodeWaitMerge = 212,
-  kSiteCombineContext = 220,
   kSitePrefillChunk = 300,
   kSitePrefillBlock = 301,
   kSitePrefillAlign = 302,
