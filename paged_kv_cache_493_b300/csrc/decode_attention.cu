@@ -12,7 +12,8 @@
 // keeps an fp32 online softmax (running max m, running sum l, unnormalised
 // output o) and the pieces are merged:
 //   M = max_j m_j,  L = sum_j l_j 2^(m_j - M),  out = sum_j o_j 2^(m_j - M) / L.
-// Scores are kept in the log2 domain (q is pre-scaled by scale * log2 e).
+// Scores are kept in the log2 domain (scaled by scale * log2 e after the
+// product; q itself is used unscaled).
 //
 // Work structure (stream-K).  Every (sequence, KV head) pair's context is
 // a run of 32-token chunks (an empty or rejected context counts as one
@@ -23,12 +24,15 @@
 // chunk counts over the sequences itself (the lengths live on the device).
 // The piece of a pair inside one slice is either the whole pair (its output
 // is written directly) or a cut piece: its partial state goes to one of the
-// block's two partial slots and the block counts it on the pair's arrival
-// counter; the block that writes the pair's last piece merges all of them
-// once its own slice is done, with all its threads (there is no second
-// kernel).  Counters carry a generation kept on the device (the last block of
-// a launch advances it), so nothing is ever reset between launches.
-// In one block:
+// block's two partial slots and is counted on the pair's arrival counter;
+// the block that brings the count to the pair's number of pieces merges all
+// of them (there is no second kernel).  A slice's trailing cut piece is
+// streamed first, so that cross-block merges happen while the streams go on
+// and every block ends on a piece that needs none.  Counters carry a launch
+// generation kept on the device (the last block of a launch to start
+// advances it), so nothing is ever reset between launches, and replays of
+// a captured graph stay correct.
+// In one block (seven warps):
 //   warp 4        producer: one lane walks the block's slice, looks up each
 //                 chunk's physical block, and issues TMA tile loads (K and V
 //                 rows of the KV head, 32 tokens x 64 dimensions per panel,
@@ -48,8 +52,14 @@
 //                 P^T by one 8x8 transpose in registers (movmatrix) per 16
 //                 tokens; the per-head running max is reduced over the eight
 //                 lanes that hold a head's tokens.  At the last chunk of a
-//                 piece the four warps merge their states and write the
-//                 output (a whole pair) or the piece's partials.
+//                 piece each warp posts its state to a shared-memory mailbox
+//                 and goes on.
+//   warp 5        merger: combines the four warps' states of each posted
+//                 piece, frees the mailbox, then writes a whole pair's output
+//                 or a cut piece's partials and counts it.
+//   warp 6        merge warp: merges the pieces of the cut pairs whose count
+//                 this block completed (reads of partials written by other
+//                 blocks: L2 round trips, kept off the consumers' path).
 // P is rounded to bf16 for the PV product (its sum l stays fp32).  V rows
 // past the context in a final, partial chunk are zeroed in shared memory
 // before the product (their pool contents may be anything).
@@ -70,7 +80,6 @@ constexpr int kProducerWarp = 4;   // TMA issue
 constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
 constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum-exp over L2)
 constexpr int kDecodeThreads = 7 * 32;
-constexpr int kPairs = 16;  // (token, head) dot products per warp step
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
