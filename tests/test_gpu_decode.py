@@ -222,3 +222,11 @@ def test_graph_replays_follow_new_inputs(cuda_device):
         replayed = W.DecodeCase(**{**case.__dict__, "q": q_host})
         assert_close(out, oracle_decode_after_store(replayed), f"replay {i}")
     no_device_error()
+
+
+def test_decode_negative_scale(cuda_device):
+    case = W.make_decode_case("neg", [1, 40, 256, 700, 3000], 16, 8, 128, 32, seed=92,
+                              scale=-0.08)
+    out, _, _ = run_decode_step(case)
+    assert_close(out, oracle_decode_after_store(case), "negative scale")
+    no_device_error()

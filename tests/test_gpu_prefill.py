@@ -115,3 +115,13 @@ def test_prefill_block_relabelling_is_invisible(cuda_device):
                               case.scale, o2)
     torch.cuda.synchronize()
     assert torch.equal(o2, out)
+
+
+def test_prefill_negative_scale(cuda_device):
+    """A negative softmax scale flips which raw score is the row maximum; the
+    kernel then tracks the raw minimum.  Ragged chunks over cached prefixes."""
+    case = W.make_prefill_case("neg", [0, 300, 77], [200, 70, 1], 16, 8, 128, 24, seed=91,
+                               scale=-0.08)
+    out, _, _ = run_prefill_step(case)
+    assert_close(out, oracle_prefill_after_store(case), "negative scale")
+    no_device_error()
