@@ -11,7 +11,9 @@ calls captured once as a CUDA graph and replayed, as a serving engine replays
 its decode step; the eager (uncaptured) time is reported beside it.
 The metric is KV GB/s (algorithmic bytes / step time) with decode tokens/s per
 layer beside it.  The long-context decode, prefix-sharing decode and chunked
-prefill workloads are measured too and reported under "other_workloads".
+prefill workloads are measured too and reported under "other_workloads", with
+the host cost of the block manager that produces the decode step's block
+tables and slot mapping.
 
 Timing: W untimed warm-up steps, then K steps bracketed by a barrier and
 cudaDeviceSynchronize; L2 (126 MB) is flushed before every step by a 256 MiB
@@ -437,6 +439,8 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
         res[name] = entry
         del bench
         torch.cuda.empty_cache()
+    if only is None:
+        res["host_block_manager"] = host_block_manager(pkv)
     if only is not None and only != "chunked_prefill_8x512":
         return res
     # Chunked prefill.
@@ -466,6 +470,39 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
         "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
         "store_ms": round(st_ms, 5), "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
     return res
+
+
+def host_block_manager(pkv, steps: int = 2000) -> dict:
+    """Host cost of producing the decode inputs: the block manager (C++, behind
+    the C ABI) admitting 128 prompts of 4096 tokens that share a 2048-token
+    prefix, then decode steps that append one token to each of the 128
+    sequences and fill the [128, max_blocks] block table and context lengths."""
+    prompts = W.shared_prefix_prompts()
+    b = len(prompts)
+    max_blocks = -(-(4096 + steps) // W.BLOCK_SIZE)
+    bm = pkv.BlockManager(8 * 1024)
+    t0 = time.perf_counter()
+    cached = [bm.allocate(s, p) for s, p in enumerate(prompts)]
+    alloc_s = time.perf_counter() - t0
+    ids = torch.arange(b, dtype=torch.int64)
+    tokens = torch.zeros(b, dtype=torch.int32)
+    slots = torch.empty(b, dtype=torch.int32)
+    tables = torch.empty(b, max_blocks, dtype=torch.int32)
+    lens = torch.empty(b, dtype=torch.int32)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        tokens.fill_(i)
+        bm.append_decode_into(ids, tokens, slots)
+        bm.block_tables_into(ids, tables, lens)
+    step_s = (time.perf_counter() - t0) / steps
+    ok = bool((lens == 4096 + steps).all()) and bm.num_free_blocks() == 8 * 1024 - (
+        2048 // W.BLOCK_SIZE + b * (-(-(4096 + steps) // W.BLOCK_SIZE) - 2048 // W.BLOCK_SIZE))
+    bm.close()
+    return {"unit": "us (host, one thread)", "num_seqs": b,
+            "allocate_us_per_prompt": round(alloc_s / b * 1e6, 2),
+            "cached_tokens_first_prompt": cached[0], "cached_tokens_others": cached[1],
+            "decode_step_us": round(step_s * 1e6, 3), "decode_steps": steps,
+            "pool_accounting_ok": ok}
 
 
 def run_single(args, rank, world, local):

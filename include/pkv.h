@@ -46,7 +46,8 @@
  *   (its output row is written as zeros), never dereferenced, and recorded
  *   in a per-device error word that pkv_get_device_error reads.
  * - There is no CPU fallback: without a usable sm_103a device every call
- *   returns PKV_ERR_CUDA.
+ *   that launches a kernel returns PKV_ERR_CUDA.  (The host block manager at
+ *   the end of this file is host code and needs no device.)
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -263,6 +264,97 @@ pkv_status pkv_set_wait_limit_ns(int64_t limit_ns);
 pkv_status pkv_profiler_enable(int32_t enable);
 pkv_status pkv_profiler_reset(void);
 pkv_status pkv_profiler_read(const char* name, double* total_ms, int64_t* launches);
+
+/*
+ * Host block manager
+ * ------------------
+ * Produces the block_tables, context_lens and slot_mapping arguments of the
+ * calls above.  It runs on the host only: every pointer below is a HOST
+ * pointer owned by the caller, no call touches a device, and the calls work
+ * without a GPU.  It manages a pool of num_blocks cache blocks of 256 slots:
+ *
+ * - Blocks are handed out from the front of a free deque, ceil(tokens / 256)
+ *   per sequence (intelliparadigm.com Nano-vLLM article, §2.1 动态分块内存管理).
+ * - Each block carries a reference count; a block is free when its count is
+ *   zero (blog.hotdry.top "1200行代码挑战vLLM", §2 内存管理策略: direct
+ *   reference counting).
+ * - Prefix cache (same article, §性能优化 1 前缀缓存): every FULL block is
+ *   registered under a 64-bit key chained over the token ids of the whole
+ *   prefix up to its end.  A new sequence whose prompt starts with cached full
+ *   blocks shares them (their counts go up) instead of getting fresh ones;
+ *   those tokens' K/V is already in the cache (ocdem.com nano-vllm article,
+ *   §2.1: sequences with a common prefix point at the same physical blocks).
+ *   A hit also compares the block's 256 stored token ids and its
+ *   predecessor's key.  Only the leading run of cached blocks is reused.
+ * - Delayed release (intelliparadigm.com article, §7.2 延迟释放策略): a block
+ *   whose count reaches zero goes to the BACK of the free deque and keeps its
+ *   cached content until it is handed out again, so a later prompt with the
+ *   same prefix still finds it.  A freed sequence releases its blocks from
+ *   last to first.
+ *
+ * Sequences are named by caller-chosen int64 ids.  Calls return
+ * PKV_ERR_INVALID_ARG for a null manager or pointer, a negative size or an
+ * unknown (or, for allocate, already present) sequence id, and
+ * PKV_ERR_NO_MEMORY when the free blocks do not suffice; a failed call
+ * changes nothing.  A manager is not thread-safe: serialise calls on it.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* Create a manager of blocks 0 .. num_blocks - 1, all free (in that order).
+ * num_blocks * 256 must fit in int32 (the slots are int32).  *out receives the
+ * manager, to be released with pkv_bm_destroy. */
+pkv_status pkv_bm_create(int32_t num_blocks, pkv_block_manager** out);
+void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Number of blocks with count zero (cached or not); 0 for a null manager. */
+int32_t pkv_bm_num_free_blocks(const pkv_block_manager* bm);
+
+/* Reference count of `block` (number of live sequences whose table holds it),
+ * or -1 for an index out of range. */
+int32_t pkv_bm_ref_count(const pkv_block_manager* bm, int32_t block);
+
+/* Add sequence seq_id with its prompt tokens[0 .. num_tokens).  Leading full
+ * blocks found in the prefix cache are shared; the rest come fresh from the
+ * free deque.  *num_cached_tokens (may be NULL) receives how many leading
+ * tokens already have their K/V in the cache (a multiple of 256): the caller
+ * stores and computes only tokens [*num_cached_tokens, num_tokens), whose
+ * slots pkv_bm_slots gives. */
+pkv_status pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                           int32_t num_tokens, int32_t* num_cached_tokens);
+
+/* Append n tokens to sequence seq_id (a prefill chunk, or one decoded token),
+ * opening new blocks as needed; a block that becomes full enters the prefix
+ * cache.  slots (may be NULL) receives the n cache slots, the slot_mapping
+ * of pkv_store_kvcache. */
+pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens, int32_t n,
+                         int32_t* slots);
+
+/* One decode step: append tokens[s] to sequence seq_ids[s] for every s
+ * (distinct, known ids) and write its slot to slot_mapping[s], the
+ * slot_mapping of that step's pkv_store_kvcache.  Fails as a whole
+ * (PKV_ERR_NO_MEMORY) when fewer blocks are free than the sequences whose
+ * last block is full.  Same as num_seqs calls of pkv_bm_append with one
+ * token each, in one call. */
+pkv_status pkv_bm_append_decode(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs,
+                                const int32_t* tokens, int32_t* slot_mapping);
+
+/* Drop sequence seq_id: every block of its table loses one count. */
+pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+
+/* Fill block_tables [num_seqs][max_blocks] (row s: the physical blocks of
+ * sequence seq_ids[s] in logical order, then -1) and context_lens[num_seqs]
+ * (its token count): the arguments of pkv_decode_attention and
+ * pkv_prefill_attention.  A sequence with more than max_blocks blocks is
+ * PKV_ERR_INVALID_ARG. */
+pkv_status pkv_bm_block_tables(const pkv_block_manager* bm, const int64_t* seq_ids,
+                               int32_t num_seqs, int32_t max_blocks, int32_t* block_tables,
+                               int32_t* context_lens);
+
+/* slots[0 .. end - begin) = cache slots of tokens [begin, end) of sequence
+ * seq_id (slot = block * 256 + position in block); end must not exceed its
+ * token count. */
+pkv_status pkv_bm_slots(const pkv_block_manager* bm, int64_t seq_id, int32_t begin, int32_t end,
+                        int32_t* slots);
 
 #ifdef __cplusplus
 }

@@ -47,6 +47,16 @@ SIGNATURES = {
     "pkv_profiler_enable": ([_I32], _I32),
     "pkv_profiler_reset": ([], _I32),
     "pkv_profiler_read": ([ctypes.c_char_p, ctypes.POINTER(_D), ctypes.POINTER(_I64)], _I32),
+    "pkv_bm_create": ([_I32, ctypes.POINTER(_P)], _I32),
+    "pkv_bm_destroy": ([_P], None),
+    "pkv_bm_num_free_blocks": ([_P], _I32),
+    "pkv_bm_ref_count": ([_P, _I32], _I32),
+    "pkv_bm_allocate": ([_P, _I64, _P, _I32, ctypes.POINTER(_I32)], _I32),
+    "pkv_bm_append": ([_P, _I64, _P, _I32, _P], _I32),
+    "pkv_bm_append_decode": ([_P, _P, _I32, _P, _P], _I32),
+    "pkv_bm_free": ([_P, _I64], _I32),
+    "pkv_bm_block_tables": ([_P, _P, _I32, _I32, _P, _P], _I32),
+    "pkv_bm_slots": ([_P, _I64, _I32, _I32, _P], _I32),
 }
 
 
@@ -242,3 +252,128 @@ def pkv_profiler_read(name: str):
     _check(load_library().pkv_profiler_read(name.encode(), ctypes.byref(ms), ctypes.byref(n)),
            "pkv_profiler_read")
     return float(ms.value), int(n.value)
+
+
+def _host_i32(values):
+    """(pointer, count) of int32 host data: a contiguous CPU int32 torch tensor
+    or numpy array is passed in place; any other sequence of ints is copied."""
+    if hasattr(values, "data_ptr") and not getattr(values, "is_cuda", True):
+        import torch
+        _need(values.dtype == torch.int32 and values.is_contiguous(),
+              "tokens: contiguous CPU int32 tensor")
+        return ctypes.c_void_p(values.data_ptr()), int(values.numel())
+    if hasattr(values, "__array_interface__"):
+        import numpy as np
+        _need(values.dtype == np.int32 and values.flags["C_CONTIGUOUS"],
+              "tokens: contiguous int32 array")
+        return ctypes.c_void_p(values.ctypes.data), int(values.size)
+    values = list(values)
+    return (ctypes.c_int32 * max(len(values), 1))(*values), len(values)
+
+
+class BlockManager:
+    """Host block manager (``pkv_bm_*``): 256-token blocks with reference
+    counts and a prefix cache; produces block tables, context lengths and slot
+    mappings.  Pure host code: works without a GPU."""
+
+    def __init__(self, num_blocks: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.pkv_bm_create(int(num_blocks), ctypes.byref(h)), "pkv_bm_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pkv_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free_blocks(self) -> int:
+        return int(self._lib.pkv_bm_num_free_blocks(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pkv_bm_ref_count(self._h, int(block)))
+
+    def allocate(self, seq_id: int, tokens) -> int:
+        """Add a sequence with its prompt; returns the number of leading tokens
+        whose K/V is already cached (a multiple of 256)."""
+        buf, n = _host_i32(tokens)
+        cached = ctypes.c_int32(0)
+        _check(self._lib.pkv_bm_allocate(self._h, int(seq_id), buf, n, ctypes.byref(cached)),
+               "pkv_bm_allocate")
+        return int(cached.value)
+
+    def append(self, seq_id: int, tokens) -> list:
+        """Append tokens to a sequence; returns their cache slots."""
+        buf, n = _host_i32(tokens)
+        slots = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pkv_bm_append(self._h, int(seq_id), buf, n, slots), "pkv_bm_append")
+        return list(slots[:n])
+
+    def append_decode(self, seq_ids, tokens) -> list:
+        """One decode step: one token per sequence; returns the slot mapping."""
+        seq_ids = [int(x) for x in seq_ids]
+        buf, n = _host_i32(tokens)
+        _need(n == len(seq_ids), "append_decode: one token per sequence")
+        ids = (ctypes.c_int64 * max(n, 1))(*seq_ids)
+        slots = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pkv_bm_append_decode(self._h, ids, n, buf, slots), "pkv_bm_append_decode")
+        return list(slots[:n])
+
+    def append_decode_into(self, seq_ids, tokens, slot_mapping) -> None:
+        """append_decode on CPU tensors: seq_ids int64 [B], tokens int32 [B];
+        fills the CPU int32 tensor slot_mapping [B] in place."""
+        import torch
+        for t, dt, name in ((seq_ids, torch.int64, "seq_ids"), (tokens, torch.int32, "tokens"),
+                            (slot_mapping, torch.int32, "slot_mapping")):
+            _need(t.device.type == "cpu" and t.dtype == dt and t.is_contiguous()
+                  and t.numel() == seq_ids.numel(), f"{name}: contiguous CPU {dt} [B]")
+        _check(self._lib.pkv_bm_append_decode(self._h, _ptr(seq_ids), seq_ids.numel(),
+                                              _ptr(tokens), _ptr(slot_mapping)),
+               "pkv_bm_append_decode")
+
+    def free(self, seq_id: int) -> None:
+        _check(self._lib.pkv_bm_free(self._h, int(seq_id)), "pkv_bm_free")
+
+    def slots(self, seq_id: int, begin: int, end: int) -> list:
+        n = max(int(end) - int(begin), 0)
+        out = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pkv_bm_slots(self._h, int(seq_id), int(begin), int(end), out),
+               "pkv_bm_slots")
+        return list(out[:n])
+
+    def block_tables(self, seq_ids, max_blocks: int):
+        """(block_tables rows as lists, context_lens list) for the sequences."""
+        seq_ids = [int(x) for x in seq_ids]
+        b, mb = len(seq_ids), int(max_blocks)
+        ids = (ctypes.c_int64 * max(b, 1))(*seq_ids)
+        tables = (ctypes.c_int32 * max(b * mb, 1))()
+        lens = (ctypes.c_int32 * max(b, 1))()
+        _check(self._lib.pkv_bm_block_tables(self._h, ids, b, mb, tables, lens),
+               "pkv_bm_block_tables")
+        return [list(tables[i * mb:(i + 1) * mb]) for i in range(b)], list(lens[:b])
+
+    def block_tables_into(self, seq_ids, block_tables, context_lens) -> None:
+        """Fill pinned or plain CPU int32 tensors block_tables [B, max_blocks]
+        and context_lens [B] in place; seq_ids is best a CPU int64 tensor
+        (then nothing is copied)."""
+        import torch
+        seq = seq_ids
+        if not (isinstance(seq, torch.Tensor) and seq.device.type == "cpu"
+                and seq.dtype == torch.int64 and seq.is_contiguous()):
+            seq = torch.as_tensor([int(x) for x in seq_ids], dtype=torch.int64)
+        _need(block_tables.device.type == "cpu" and block_tables.dtype == torch.int32
+              and block_tables.is_contiguous() and block_tables.dim() == 2
+              and block_tables.shape[0] == seq.numel(), "block_tables: CPU int32 [B, max_blocks]")
+        _need(context_lens.device.type == "cpu" and context_lens.dtype == torch.int32
+              and context_lens.is_contiguous() and context_lens.numel() == seq.numel(),
+              "context_lens: CPU int32 [B]")
+        _check(self._lib.pkv_bm_block_tables(self._h, _ptr(seq), seq.numel(),
+                                             block_tables.shape[1], _ptr(block_tables),
+                                             _ptr(context_lens)), "pkv_bm_block_tables")

@@ -250,3 +250,100 @@ WORKLOADS = {
     "prefix_decode_b64": prefix_decode,
     "chunked_prefill_8x512": chunked_prefill,
 }
+
+
+def block_manager_trace(seed: int, num_ops: int, num_prefixes: int = 4, vocab: int = 64,
+                        max_live: int = 24, invalid_prob: float = 0.03) -> List[tuple]:
+    """A seeded sequence of block-manager calls with a serving-like structure.
+
+    Each new request's prompt is one of a few shared "system" prefixes (some a
+    whole number of 256-token blocks, some not), or none, followed by its own
+    tokens; live sequences grow by prefill chunks and single decoded tokens and
+    are freed at random.  The ops are tuples:
+
+      ("allocate", seq_id, tokens)   ("append", seq_id, tokens)
+      ("free", seq_id)               ("slots", seq_id, begin, end)
+      ("tables", [seq_id, ...], max_blocks)
+      ("decode", [seq_id, ...], tokens)   (one token for each sequence)
+
+    A small share of ops is invalid on purpose (unknown or repeated sequence
+    ids, a token range past the end, a table narrower than a sequence, a
+    decode step naming a sequence twice).  Only
+    token ids and op choices are drawn here: which blocks the calls hand out
+    is for the manager under test to decide.
+    """
+    g = _gen(seed)
+
+    def randint(lo: int, hi: int) -> int:  # inclusive
+        return int(torch.randint(lo, hi + 1, (1,), generator=g))
+
+    def tokens(n: int) -> List[int]:
+        return torch.randint(0, vocab, (n,), generator=g).tolist() if n else []
+
+    prefix_lens = [256, 512, 300, 700, 1024, 130][:num_prefixes]
+    prefixes = [tokens(n) for n in prefix_lens]
+    live = {}  # seq id -> token count
+    next_id = 0
+    ops: List[tuple] = []
+    for _ in range(num_ops):
+        r = float(torch.rand((), generator=g))
+        if r < invalid_prob:
+            kind = randint(0, 4)
+            if kind == 0:
+                ops.append(("free", next_id + 1000))
+            elif kind == 1 and live:
+                ops.append(("allocate", list(live)[0], tokens(3)))
+            elif kind == 2 and live:
+                s = list(live)[randint(0, len(live) - 1)]
+                ops.append(("slots", s, 0, live[s] + 1))
+            elif kind == 3 and live:
+                s = max(live, key=live.get)
+                ops.append(("tables", [s], max(live[s] - 1, 0) // BLOCK_SIZE))
+            elif live:
+                s = list(live)[0]
+                ops.append(("decode", [s, s], tokens(2)))
+            continue
+        if not live or (len(live) < max_live and r < 0.30):
+            pick = randint(0, len(prefixes))
+            prompt = (prefixes[pick] if pick < len(prefixes) else []) + tokens(randint(0, 600))
+            ops.append(("allocate", next_id, prompt))
+            live[next_id] = len(prompt)
+            next_id += 1
+        elif r < 0.45:
+            s = list(live)[randint(0, len(live) - 1)]
+            ops.append(("free", s))
+            del live[s]
+        elif r < 0.55:
+            s = list(live)[randint(0, len(live) - 1)]
+            chunk = tokens(randint(1, 400))
+            ops.append(("append", s, chunk))
+            live[s] += len(chunk)
+        elif r < 0.70:
+            s = list(live)[randint(0, len(live) - 1)]
+            ops.append(("append", s, tokens(1)))
+            live[s] += 1
+        elif r < 0.85:
+            ids = [s for s in torch.randperm(len(live), generator=g).tolist()]
+            ids = [list(live)[i] for i in ids[:randint(1, len(live))]]
+            ops.append(("decode", ids, tokens(len(ids))))
+            for s in ids:
+                live[s] += 1
+        elif r < 0.93:
+            s = list(live)[randint(0, len(live) - 1)]
+            b = randint(0, live[s])
+            ops.append(("slots", s, b, randint(b, live[s])))
+        else:
+            ids = list(live)
+            width = max(-(-n // BLOCK_SIZE) for n in live.values()) + randint(0, 2)
+            ops.append(("tables", ids, width))
+    return ops
+
+
+def shared_prefix_prompts(seed: int = 1006, num_seqs: int = 128, prefix_len: int = 2048,
+                          prompt_len: int = 4096, vocab: int = 32000) -> List[torch.Tensor]:
+    """num_seqs int32 prompts of prompt_len token ids: one shared system prefix
+    of prefix_len ids, then each prompt's own ids (uniform over the vocab)."""
+    g = _gen(seed)
+    prefix = torch.randint(0, vocab, (prefix_len,), generator=g, dtype=torch.int32)
+    return [torch.cat([prefix, torch.randint(0, vocab, (prompt_len - prefix_len,), generator=g,
+                                             dtype=torch.int32)]) for _ in range(num_seqs)]
