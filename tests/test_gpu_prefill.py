@@ -125,3 +125,77 @@ def test_prefill_negative_scale(cuda_device):
     out, _, _ = run_prefill_step(case)
     assert_close(out, oracle_prefill_after_store(case), "negative scale")
     no_device_error()
+
+
+def _sample_rows(cu, num_heads, per_seq=24):
+    rows = []
+    for s in range(len(cu) - 1):
+        c0, c1 = int(cu[s]), int(cu[s + 1])
+        if c1 <= c0:
+            continue
+        picks = {c0, c1 - 1} | {c0 + (37 * k + 5 * s) % (c1 - c0) for k in range(per_seq)}
+        rows += [(t, (t * 7 + s) % num_heads) for t in sorted(picks)]
+        rows += [(c1 - 1, h) for h in range(num_heads)]
+    return rows
+
+
+def test_prefill_long_context_single_sequence(cuda_device):
+    """One 256-token chunk over 8192 cached keys (about 5% of its rows not
+    stored): few tiles, each with a long loop over 130 key tiles, and a
+    softmax whose running max moves across many tiles."""
+    case = W.make_prefill_case("long", [8192], [256], 16, 8, 128, 40, seed=21, skip_prob=0.05)
+    out, _, _ = run_prefill_step(case)
+    rows = _sample_rows(case.cu_seqlens_q, 16, per_seq=40)
+    ref = oracle_prefill_after_store(case, rows=rows)
+    assert_close(torch.stack([out[t, h] for t, h in rows]), ref, "long sequence")
+    no_device_error()
+
+
+def test_prefill_graph_replays_follow_new_inputs(cuda_device):
+    """Store + prefill captured once in a CUDA graph (as an engine replays a
+    captured step), replayed over three query batches written into the
+    captured buffers: every replay must give that batch's attention."""
+    case = W.make_prefill_case("pgraph", [3000, 100, 700], [300, 200, 64], 16, 8, 128, 64, seed=31)
+    q, kc, vc, bt, cl = (dev(case.q), *cache_to_device(case.cache))
+    kn, vn, sm, cu = dev(case.k_new), dev(case.v_new), dev(case.slot_mapping), dev(case.cu_seqlens_q)
+    out = torch.empty_like(q)
+    pkv.pkv_reserve_workspace(case.num_seqs, 16, 128, bt.shape[1])
+
+    def step():
+        pkv.pkv_store_kvcache(kn, vn, sm, kc, vc)
+        pkv.pkv_prefill_attention(q, kc, vc, bt, cu, cl, case.scale, out)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(78)
+    rows = _sample_rows(case.cu_seqlens_q, 16)
+    for i in range(3):
+        q_host = torch.randn(case.q.shape, generator=gen).to(torch.bfloat16)
+        q.copy_(q_host)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        replayed = W.PrefillCase(**{**case.__dict__, "q": q_host})
+        ref = oracle_prefill_after_store(replayed, rows=rows)
+        assert_close(torch.stack([out[t, h] for t, h in rows]), ref, f"replay {i}")
+    no_device_error()
+
+
+def test_prefill_batch_of_many_tiles(cuda_device):
+    """16 chunks of 512 over 1024 cached keys: 1024 tiles (128-row tile x KV
+    head), more than three waves of two blocks per SM."""
+    case = W.make_prefill_case("waves", [1024] * 16, [512] * 16, 16, 8, 128, 112, seed=41,
+                               skip_prob=0.05)
+    out, _, _ = run_prefill_step(case)
+    rows = _sample_rows(case.cu_seqlens_q, 16, per_seq=10)
+    ref = oracle_prefill_after_store(case, rows=rows)
+    assert_close(torch.stack([out[t, h] for t, h in rows]), ref, "waves then tail")
+    no_device_error()
