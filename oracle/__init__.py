@@ -57,6 +57,12 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_prefill.argtypes = [P, P, P, I64, P, I32, P, P, I32, I32, I32, I32, D, P, I32, P]
         _lib.oracle_bf16_to_f64.argtypes = [P, I64, P]
         _lib.oracle_bf16_to_f64.restype = None
+        _lib.oracle_quantize_row.argtypes = [P, I32, P, P]
+        _lib.oracle_quantize_row.restype = None
+        _lib.oracle_store_kvcache_int8.argtypes = [P, P, I64, I64, P, I64, P, P, P, P, I64, I32, I32]
+        _lib.oracle_gather_int8.argtypes = [P, P, P, P, I64, I32, I32, P, I32, I32, P, P]
+        _lib.oracle_decode_int8.argtypes = [P, P, P, P, P, I64, P, I32, P, I32, I32, I32, I32, D,
+                                            P, I32, P]
     return _lib
 
 
@@ -170,4 +176,74 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
     _check(lib().oracle_prefill(_ptr(qb), _ptr(kb), _ptr(vb), nb,
                                 _ptr(bt), int(bt.shape[1]), _ptr(cu), _ptr(cl), int(cu.numel() - 1),
                                 hq, hkv, d, float(scale), rptr, nr, _ptr(out)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache: codes int8 [num_blocks, 256, Hkv, D], scales float32
+# [num_blocks, 256, Hkv]; a value is code * scale.
+# ---------------------------------------------------------------------------
+
+def quantize_rows(x: torch.Tensor) -> Tuple[np.ndarray, np.ndarray]:
+    """bf16 [..., D] -> (int8 codes [..., D], float32 scales [...]), one scale per row."""
+    xb = _bits(x).reshape(-1, x.shape[-1])
+    n, d = xb.shape
+    codes = np.zeros((n, d), dtype=np.int8)
+    scales = np.zeros(n, dtype=np.float32)
+    for i in range(n):
+        lib().oracle_quantize_row(ctypes.c_void_p(xb.data_ptr() + 2 * i * d), d,
+                                  ctypes.c_void_p(codes.ctypes.data + i * d),
+                                  ctypes.c_void_p(scales.ctypes.data + 4 * i))
+    return codes.reshape(tuple(x.shape)), scales.reshape(tuple(x.shape[:-1]))
+
+
+def store_kvcache_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping, k_codes, v_codes,
+                       k_scales, v_scales):
+    """Returns new (k_codes, v_codes, k_scales, v_scales) CPU tensors; inputs unchanged."""
+    nb, bs, hkv, d = k_codes.shape
+    kc, vc = k_codes.clone().contiguous(), v_codes.clone().contiguous()
+    ks, vs = k_scales.clone().contiguous(), v_scales.clone().contiguous()
+    kb, vb, sm = _bits(k), _bits(v), _i32(slot_mapping)
+    _check(lib().oracle_store_kvcache_int8(_ptr(kb), _ptr(vb), hkv * d, hkv * d, _ptr(sm),
+                                           int(sm.numel()), _ptr(kc), _ptr(vc), _ptr(ks),
+                                           _ptr(vs), nb, hkv, d))
+    return kc, vc, ks, vs
+
+
+def gather_int8(k_codes, v_codes, k_scales, v_scales, block_table_row,
+                context_len: int) -> Tuple[np.ndarray, np.ndarray]:
+    nb, bs, hkv, d = k_codes.shape
+    row = _i32(block_table_row)
+    n = max(int(context_len), 1)
+    K = np.zeros((n, hkv, d), dtype=np.float64)
+    V = np.zeros((n, hkv, d), dtype=np.float64)
+    kc, vc = k_codes.contiguous(), v_codes.contiguous()
+    ks, vs = k_scales.contiguous(), v_scales.contiguous()
+    _check(lib().oracle_gather_int8(_ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb, hkv, d,
+                                    _ptr(row), int(row.numel()), int(context_len), _ptr(K),
+                                    _ptr(V)))
+    return K[:context_len], V[:context_len]
+
+
+def decode_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tables,
+                context_lens, scale: float,
+                rows: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """Decode over an INT8 cache: full [B, Hq, D] output, or [len(rows), D]."""
+    b, hq, d = q.shape
+    nb, bs, hkv, d2 = k_codes.shape
+    assert d == d2 and k_codes.dtype == torch.int8 and k_scales.dtype == torch.float32
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    if rows is None:
+        out = np.zeros((b, hq, d), dtype=np.float64)
+        rptr, nr = None, 0
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((r.shape[0], d), dtype=np.float64)
+        rptr, nr = _ptr(r), r.shape[0]
+    kc, vc = k_codes.contiguous(), v_codes.contiguous()
+    ks, vs = k_scales.contiguous(), v_scales.contiguous()
+    qb = _bits(q)
+    _check(lib().oracle_decode_int8(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb,
+                                    _ptr(bt), int(bt.shape[1]), _ptr(cl), b, hq, hkv, d,
+                                    float(scale), rptr, nr, _ptr(out)))
     return out

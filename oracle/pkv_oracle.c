@@ -97,6 +97,61 @@ int oracle_store_kvcache(const uint16_t* k, const uint16_t* v, int64_t k_row_str
 }
 
 /*
+ * INT8 KV cache (intelliparadigm.com article §2.2, "kv_cache_dtype: int8";
+ * ocdem.com article §4.1 KV Cache 量化): each (token, KV head) row of
+ * head_dim values is stored as int8 codes with one binary32 scale.  The
+ * pages give no formula; this is symmetric absmax quantisation:
+ *   scale = max_d |x_d| / 127,  code_d = nearest(x_d / scale), ties to even,
+ * both decided in binary32 (the precision the codes are decided in on the
+ * GPU too), codes in [-127, 127]; an all-zero row has scale 0 and zero
+ * codes.  The value a code stands for is code * scale.
+ */
+void oracle_quantize_row(const uint16_t* x, int32_t n, int8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int32_t d = 0; d < n; ++d) {
+    const float a = fabsf((float)widen_bf16(x[d]));
+    if (a > amax) amax = a;
+  }
+  const float s = amax / 127.0f;
+  *scale = s;
+  for (int32_t d = 0; d < n; ++d) {
+    long c = 0;
+    if (s > 0.0f) c = lrintf((float)widen_bf16(x[d]) / s);
+    if (c > 127) c = 127;
+    if (c < -127) c = -127;
+    codes[d] = (int8_t)c;
+  }
+}
+
+/*
+ * INT8 store: row i of k and v, head h, is quantised into cache slot
+ * slot_mapping[i]: codes at k_codes[slot][h][:] and its scale at
+ * k_scales[slot][h] (the same for v); slot -1 skips the row.
+ */
+int oracle_store_kvcache_int8(const uint16_t* k, const uint16_t* v, int64_t k_row_stride,
+                              int64_t v_row_stride, const int32_t* slot_mapping,
+                              int64_t num_tokens, int8_t* k_codes, int8_t* v_codes,
+                              float* k_scales, float* v_scales, int64_t num_blocks,
+                              int32_t num_kv_heads, int32_t head_dim) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks < 0)
+    return ORACLE_BAD_ARG;
+  const int64_t num_slots = num_blocks * ORACLE_BLOCK;
+  for (int64_t i = 0; i < num_tokens; ++i) {
+    const int64_t slot = slot_mapping[i];
+    if (slot == -1) continue;
+    if (slot < 0 || slot >= num_slots) return ORACLE_BAD_SLOT;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t r = slot * num_kv_heads + h;
+      oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,
+                          k_codes + r * head_dim, k_scales + r);
+      oracle_quantize_row(v + i * v_row_stride + (int64_t)h * head_dim, head_dim,
+                          v_codes + r * head_dim, v_scales + r);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
  * Gather (ocdem.com article §2.1): logical token t of a sequence lives in
  * physical block block_table[t / 256] at offset t % 256.  Produces
  * contiguous K and V of shape [context_len][num_kv_heads][head_dim].
@@ -114,6 +169,33 @@ int oracle_gather(const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_
     for (int64_t e = 0; e < row; ++e) {
       K[(int64_t)t * row + e] = widen_bf16(k_cache[slot * row + e]);
       V[(int64_t)t * row + e] = widen_bf16(v_cache[slot * row + e]);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * Gather of an INT8 cache: as oracle_gather, each value being
+ * code * scale of its (slot, KV head) row (exact in double).
+ */
+int oracle_gather_int8(const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
+                       const float* v_scales, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_dim, const int32_t* block_table, int32_t max_blocks,
+                       int32_t context_len, double* K, double* V) {
+  if (context_len < 0) return ORACLE_BAD_CONTEXT;
+  if ((int64_t)context_len > (int64_t)max_blocks * ORACLE_BLOCK) return ORACLE_BAD_CONTEXT;
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  for (int32_t t = 0; t < context_len; ++t) {
+    const int64_t block = block_table[t / ORACLE_BLOCK];
+    if (block < 0 || block >= num_blocks) return ORACLE_BAD_BLOCK;
+    const int64_t slot = block * ORACLE_BLOCK + t % ORACLE_BLOCK;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t r = slot * num_kv_heads + h;
+      const double ks = (double)k_scales[r], vs = (double)v_scales[r];
+      for (int32_t d = 0; d < head_dim; ++d) {
+        K[(int64_t)t * row + (int64_t)h * head_dim + d] = (double)k_codes[r * head_dim + d] * ks;
+        V[(int64_t)t * row + (int64_t)h * head_dim + d] = (double)v_codes[r * head_dim + d] * vs;
+      }
     }
   }
   return ORACLE_OK;
@@ -181,11 +263,31 @@ static int check_heads(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_d
  * (sequence, q head) pairs listed in rows[2*i], rows[2*i+1] are computed and
  * out is [n_rows][head_dim]; otherwise out is [num_seqs][num_q_heads][head_dim].
  */
-int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                  int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
-                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                  int32_t num_kv_heads, int32_t head_dim, double scale,
-                  const int32_t* rows, int32_t n_rows, double* out) {
+/* The cache decode reads: bf16 (k, v) or INT8 (codes and scales). */
+typedef struct {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int8_t* k_codes;
+  const int8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+} CacheSource;
+
+static int gather_from(const CacheSource* c, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_dim, const int32_t* block_table, int32_t max_blocks,
+                       int32_t context_len, double* K, double* V) {
+  if (c->k)
+    return oracle_gather(c->k, c->v, num_blocks, num_kv_heads, head_dim, block_table,
+                         max_blocks, context_len, K, V);
+  return oracle_gather_int8(c->k_codes, c->v_codes, c->k_scales, c->v_scales, num_blocks,
+                            num_kv_heads, head_dim, block_table, max_blocks, context_len, K, V);
+}
+
+static int decode_from(const uint16_t* q, const CacheSource* cache, int64_t num_blocks,
+                       const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, double scale,
+                       const int32_t* rows, int32_t n_rows, double* out) {
   int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
   if (rc) return rc;
   const int32_t group = num_q_heads / num_kv_heads;
@@ -210,8 +312,8 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
       rc = ORACLE_NO_MEMORY;
       break;
     }
-    rc = oracle_gather(k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                       block_tables + (int64_t)s * max_blocks, max_blocks, ctx, K, V);
+    rc = gather_from(cache, num_blocks, num_kv_heads, head_dim,
+                     block_tables + (int64_t)s * max_blocks, max_blocks, ctx, K, V);
     for (int32_t h = 0; h < num_q_heads && rc == ORACLE_OK; ++h) {
       double* dst = NULL;
       int32_t first = -1;
@@ -232,6 +334,29 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
   }
   free(qrow);
   return rc;
+}
+
+int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                  int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
+                  const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                  int32_t num_kv_heads, int32_t head_dim, double scale,
+                  const int32_t* rows, int32_t n_rows, double* out) {
+  const CacheSource c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+  return decode_from(q, &c, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, scale, rows, n_rows, out);
+}
+
+/* Decode over an INT8 cache (codes [num_blocks][256][Hkv][D], scales
+ * [num_blocks][256][Hkv]): the same attention on the values the codes stand for. */
+int oracle_decode_int8(const uint16_t* q, const int8_t* k_codes, const int8_t* v_codes,
+                       const float* k_scales, const float* v_scales, int64_t num_blocks,
+                       const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, double scale,
+                       const int32_t* rows, int32_t n_rows, double* out) {
+  const CacheSource c = {NULL, NULL, k_codes, v_codes, k_scales, v_scales};
+  return decode_from(q, &c, num_blocks, block_tables, max_blocks, context_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, scale, rows, n_rows, out);
 }
 
 /*
