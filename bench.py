@@ -439,6 +439,9 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
         res[name] = entry
         del bench
         torch.cuda.empty_cache()
+    if only is None or only == "qwen_decode_b128_int8":
+        res["qwen_decode_b128_int8"] = int8_decode_workload(pkv, steps, flush, peaks, rank)
+        torch.cuda.empty_cache()
     if only is None:
         res["host_block_manager"] = host_block_manager(pkv)
     if only is not None and only != "chunked_prefill_8x512":
@@ -470,6 +473,46 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
         "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
         "store_ms": round(st_ms, 5), "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
     return res
+
+
+def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
+    """The 128-sequence decode step over the INT8 cache: quantising store of
+    the new rows, then decode (split + combine kernels).  The INT8 pool holds
+    the same tokens as the bf16 pool: the quantising store is run over every
+    slot of it first."""
+    case = W.qwen_decode(seed=replica_seed(1002, rank))
+    c = case.cache
+    nb, bs, hkv, d = (int(x) for x in c.k_cache.shape)
+    kc = torch.empty((nb, bs, hkv, d), dtype=torch.int8, device="cuda")
+    vc = torch.empty_like(kc)
+    ks = torch.empty((nb, bs, hkv), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    kb, vb = to_dev(c.k_cache).view(nb * bs, hkv, d), to_dev(c.v_cache).view(nb * bs, hkv, d)
+    every = torch.arange(nb * bs, dtype=torch.int32, device="cuda")
+    pkv.pkv_store_kvcache_int8(kb, vb, every, kc, vc, ks, vs)
+    del kb, vb, every
+    q, kn, vn, sm = to_dev(case.q), to_dev(case.k_new), to_dev(case.v_new), to_dev(case.slot_mapping)
+    bt, cl = to_dev(c.block_tables), to_dev(c.context_lens)
+    out = torch.empty_like(q)
+
+    def step():
+        pkv.pkv_store_kvcache_int8(kn, vn, sm, kc, vc, ks, vs)
+        pkv.pkv_decode_attention_int8(q, kc, vc, ks, vs, bt, cl, case.scale, out)
+
+    for _ in range(3):
+        step()
+    kt = kernel_times(pkv, step, steps, flush, ["store_kvcache_int8", "decode_int8"])
+    per, _ = time_steps(step, steps, flush)
+    ms = sum(per) / len(per)
+    dec_ms = kt["decode_int8"][0] / max(kt["decode_int8"][1], 1)
+    kv = int(c.context_lens.sum()) * hkv * (2 * d + 2 * 4)  # codes + one fp32 scale per row, K and V
+    dec_bytes = kv + case.q.numel() * 2 * 2 + (c.block_tables.numel() + c.context_lens.numel()) * 4
+    gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    return {"step_ms": round(ms, 5), "decode_ms": round(dec_ms, 5), "kv_bytes": kv,
+            "decode_bytes": dec_bytes, "decode_gbs": round(gbs, 2),
+            "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+            "tokens_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1),
+            "kernels": "store_kvcache_int8; decode_int8 = split + combine"}
 
 
 def host_block_manager(pkv, steps: int = 2000) -> dict:
@@ -591,7 +634,7 @@ def main(argv=None):
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--workload", default=MAIN_WORKLOAD,
                     choices=[MAIN_WORKLOAD, "long_decode_32k", "prefix_decode_b64",
-                             "chunked_prefill_8x512"],
+                             "chunked_prefill_8x512", "qwen_decode_b128_int8"],
                     help="run one non-default workload alone (for profiling) and print its entry")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "pkv":

@@ -219,6 +219,50 @@ const char* pkv_status_string(pkv_status status);
 const char* pkv_version(void);
 
 /*
+ * INT8 KV cache (intelliparadigm.com Nano-vLLM article §2.2,
+ * "kv_cache_dtype: int8"; ocdem.com nano-vllm article §4.1 KV Cache 量化):
+ * half the bytes of the bf16 cache for the same tokens.  Every (token, KV
+ * head) row of head_dim values is held as int8 codes and one binary32 scale:
+ *   scale = max_d |x_d| / 127,  code_d = nearest(x_d / scale), ties to even,
+ * with IEEE binary32 division (codes in [-127, 127]; an all-zero row has
+ * scale 0); a code stands for code * scale.  (The pages give no formula:
+ * this is symmetric absmax quantisation per row.)
+ *   k_codes, v_codes    int8 [num_blocks][256][num_kv_heads][head_dim]
+ *   k_scales, v_scales  float32 [num_blocks][256][num_kv_heads]
+ * all device pointers, 16-byte aligned, owned by the caller.
+ *
+ * pkv_store_kvcache_int8 -- as pkv_store_kvcache (same k, v, strides and
+ * slot_mapping rules, slot -1 skipped, out-of-range slots skipped and
+ * reported as PKV_ERR_DEVICE_CHECK), writing each row's codes and scale.
+ * The codes and scales are exactly those the definition above gives.
+ * head_dim 64 or 128.
+ */
+pkv_status pkv_store_kvcache_int8(const void* k, const void* v, int64_t k_row_stride,
+                                  int64_t v_row_stride, const int32_t* slot_mapping,
+                                  int64_t num_tokens, int8_t* k_codes, int8_t* v_codes,
+                                  float* k_scales, float* v_scales, int64_t num_blocks,
+                                  int32_t num_kv_heads, int32_t head_dim, pkv_stream_t stream);
+
+/*
+ * pkv_decode_attention_int8 -- pkv_decode_attention over an INT8 cache: the
+ * same arguments, with the bf16 cache replaced by codes and scales, and the
+ * same result on the values the codes stand for (fp32 accumulation, bf16
+ * output).  A split-K kernel (512-token splits of each context, the G query
+ * heads of a KV head together) followed by a log-sum-exp combine kernel;
+ * the partial states live in the library's decode workspace (allocated on
+ * first need), so overlapping calls on different streams must be
+ * serialised by the caller.  Out-of-range block ids or context lengths give
+ * a zero output for the sequence and PKV_ERR_DEVICE_CHECK.
+ */
+pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const int8_t* k_codes,
+                                     const int8_t* v_codes, const float* k_scales,
+                                     const float* v_scales, int64_t num_blocks,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     float scale, void* out, pkv_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's error
  * word.  *code receives PKV_OK or the first PKV_ERR_DEVICE_CHECK /
  * PKV_ERR_TIMEOUT recorded since the last read; *info (may be NULL) an
@@ -258,7 +302,8 @@ pkv_status pkv_set_wait_limit_ns(int64_t limit_ns);
  * Kernel timing: while enabled, every kernel launch of the library is
  * bracketed by CUDA events on its own stream.  pkv_profiler_read
  * synchronises the recorded events and returns, for kernel `name`
- * ("store_kvcache", "decode", "prefill"), the summed
+ * ("store_kvcache", "decode", "prefill", "store_kvcache_int8",
+ * "decode_int8"), the summed
  * duration in milliseconds and the launch count since the last reset.
  */
 pkv_status pkv_profiler_enable(int32_t enable);

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_bf16_to_f64.restype = None
         _lib.oracle_quantize_row.argtypes = [P, I32, P, P]
         _lib.oracle_quantize_row.restype = None
+        _lib.oracle_quantize_rows.argtypes = [P, I64, I32, P, P]
+        _lib.oracle_quantize_rows.restype = None
         _lib.oracle_store_kvcache_int8.argtypes = [P, P, I64, I64, P, I64, P, P, P, P, I64, I32, I32]
         _lib.oracle_gather_int8.argtypes = [P, P, P, P, I64, I32, I32, P, I32, I32, P, P]
         _lib.oracle_decode_int8.argtypes = [P, P, P, P, P, I64, P, I32, P, I32, I32, I32, I32, D,
@@ -190,10 +192,7 @@ def quantize_rows(x: torch.Tensor) -> Tuple[np.ndarray, np.ndarray]:
     n, d = xb.shape
     codes = np.zeros((n, d), dtype=np.int8)
     scales = np.zeros(n, dtype=np.float32)
-    for i in range(n):
-        lib().oracle_quantize_row(ctypes.c_void_p(xb.data_ptr() + 2 * i * d), d,
-                                  ctypes.c_void_p(codes.ctypes.data + i * d),
-                                  ctypes.c_void_p(scales.ctypes.data + 4 * i))
+    lib().oracle_quantize_rows(_ptr(xb), n, d, _ptr(codes), _ptr(scales))
     return codes.reshape(tuple(x.shape)), scales.reshape(tuple(x.shape[:-1]))
 
 

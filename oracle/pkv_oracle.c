@@ -123,6 +123,13 @@ void oracle_quantize_row(const uint16_t* x, int32_t n, int8_t* codes, float* sca
   }
 }
 
+/* n_rows consecutive rows of n values each, one after another. */
+void oracle_quantize_rows(const uint16_t* x, int64_t n_rows, int32_t n, int8_t* codes,
+                          float* scales) {
+  for (int64_t r = 0; r < n_rows; ++r)
+    oracle_quantize_row(x + r * n, n, codes + r * n, scales + r);
+}
+
 /*
  * INT8 store: row i of k and v, head h, is quantised into cache slot
  * slot_mapping[i]: codes at k_codes[slot][h][:] and its scale at

@@ -38,6 +38,10 @@ SIGNATURES = {
                                _I32, _F, _P, _P], _I32),
     "pkv_decode_attention_noalloc": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
                                       _I32, _F, _P, _P], _I32),
+    "pkv_store_kvcache_int8": ([_P, _P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32,
+                                _P], _I32),
+    "pkv_decode_attention_int8": ([_P, _I64, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
+                                   _I32, _I32, _F, _P, _P], _I32),
     "pkv_status_string": ([_I32], ctypes.c_char_p),
     "pkv_version": ([], ctypes.c_char_p),
     "pkv_get_device_error": ([_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)], _I32),
@@ -207,6 +211,51 @@ def pkv_prefill_attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, conte
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
         _ptr(cu_seqlens_q), _ptr(context_lens), b, t, hq, hkv, d, float(scale), _ptr(out),
         _stream(stream)), "pkv_prefill_attention")
+
+
+def _int8_cache(k_codes, v_codes, k_scales, v_scales):
+    import torch
+    for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _need(t.is_cuda and t.dtype == torch.int8 and t.dim() == 4 and t.is_contiguous()
+              and t.shape[1] == BLOCK_SIZE, f"{n}: contiguous int8 CUDA [NB, 256, Hkv, D]")
+    for t, n in ((k_scales, "k_scales"), (v_scales, "v_scales")):
+        _need(t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+              and tuple(t.shape) == tuple(k_codes.shape[:3]), f"{n}: contiguous float32 CUDA [NB, 256, Hkv]")
+    _need(k_codes.shape == v_codes.shape, "k_codes and v_codes shapes differ")
+    nb, _, hkv, d = k_codes.shape
+    return int(nb), int(hkv), int(d)
+
+
+def pkv_store_kvcache_int8(k, v, slot_mapping, k_codes, v_codes, k_scales, v_scales,
+                           stream=None) -> None:
+    """Quantise rows k, v [N, Hkv, D] into the INT8 cache at slot_mapping (-1 skips)."""
+    nb, hkv, d = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    ks, vs = _rows(k, "k", hkv, d), _rows(v, "v", hkv, d)
+    _i32(slot_mapping, "slot_mapping")
+    _need(slot_mapping.numel() == k.shape[0] == v.shape[0], "row counts differ")
+    _check(load_library().pkv_store_kvcache_int8(
+        _ptr(k), _ptr(v), ks, vs, _ptr(slot_mapping), k.shape[0], _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scales), _ptr(v_scales), nb, hkv, d, _stream(stream)), "pkv_store_kvcache_int8")
+
+
+def pkv_decode_attention_int8(q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                              scale: float, out, stream=None) -> None:
+    """Decode over the INT8 cache; out bf16 [B, Hq, D] is written."""
+    import torch
+    nb, hkv, d = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    _need(q.dim() == 3, "q: [B, Hq, D]")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    qs = _rows(q, "q", hq, d)
+    _i32(block_tables, "block_tables")
+    _i32(context_lens, "context_lens")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == b and context_lens.numel() == b,
+          "block_tables [B, max_blocks], context_lens [B]")
+    _need(out.is_cuda and out.dtype == torch.bfloat16 and out.is_contiguous()
+          and tuple(out.shape) == (b, hq, d), "out: contiguous bf16 CUDA [B, Hq, D]")
+    _check(load_library().pkv_decode_attention_int8(
+        _ptr(q), qs, _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), nb,
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), b, hq, hkv, d,
+        float(scale), _ptr(out), _stream(stream)), "pkv_decode_attention_int8")
 
 
 def pkv_get_device_error(stream=None):

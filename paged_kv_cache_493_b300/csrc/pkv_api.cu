@@ -306,6 +306,87 @@ pkv_status pkv_store_kvcache(const void* k, const void* v, int64_t k_row_stride,
       timed_launch("store_kvcache", s, [&] { return pkv::launch_store_kvcache(a, s); }));
 }
 
+pkv_status pkv_store_kvcache_int8(const void* k, const void* v, int64_t k_row_stride,
+                                  int64_t v_row_stride, const int32_t* slot_mapping,
+                                  int64_t num_tokens, int8_t* k_codes, int8_t* v_codes,
+                                  float* k_scales, float* v_scales, int64_t num_blocks,
+                                  int32_t num_kv_heads, int32_t head_dim, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!k_codes || !v_codes || !k_scales || !v_scales) return PKV_ERR_INVALID_ARG;
+  if (num_tokens > 0 && (!k || !v || !slot_mapping)) return PKV_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_row_stride < row || v_row_stride < row) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if ((k_row_stride * 2) % 16 || (v_row_stride * 2) % 16) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_codes) || !aligned16(v_codes) ||
+      !aligned16(k_scales) || !aligned16(v_scales))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_blocks > (int64_t{1} << 31) / pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  pkv_status st;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    ds = device_state(&st);
+  }
+  if (!ds) return st;
+  if (num_tokens == 0) return PKV_OK;
+  pkv::StoreI8Args a{k, v, k_row_stride, v_row_stride, slot_mapping, num_tokens, k_codes,
+                     v_codes, k_scales, v_scales, num_blocks, num_kv_heads, head_dim, ds->err};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed_launch("store_kvcache_int8", s,
+                                  [&] { return pkv::launch_store_kvcache_int8(a, s); }));
+}
+
+pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const int8_t* k_codes,
+                                     const int8_t* v_codes, const float* k_scales,
+                                     const float* v_scales, int64_t num_blocks,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* context_lens, int32_t num_seqs,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     float scale, void* out, pkv_stream_t stream) {
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_codes, v_codes, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  if (!k_scales || !v_scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_scales) || !aligned16(v_scales)) return PKV_ERR_UNSUPPORTED;
+  pkv::DecodeI8Args a{};
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0) return PKV_OK;
+    a.splits = pkv::decode_int8_splits(max_blocks_per_seq);
+    st = ensure_workspace(ds,
+                          pkv::decode_int8_partial_bytes(num_seqs, num_kv_heads, a.splits,
+                                                         num_q_heads / num_kv_heads, head_dim),
+                          0);
+    if (st != PKV_OK) return st;
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.k_codes = k_codes;
+    a.v_codes = v_codes;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.part = ds->ws;
+    a.err = ds->err;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(
+      timed_launch("decode_int8", s, [&] { return pkv::launch_decode_int8(a, s); }));
+}
+
 pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
                                 const void* v_cache, int64_t num_blocks,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,

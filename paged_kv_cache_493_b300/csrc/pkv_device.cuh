@@ -20,11 +20,14 @@ constexpr int kErrTimeout = 5;
 // Site codes stored beside the error code, for diagnostics.
 enum ErrSite : int {
   kSiteStoreSlot = 100,
+  kSiteStoreI8Slot = 101,
   kSiteDecodeContext = 200,
   kSiteDecodeBlock = 201,
   kSiteDecodeWaitFull = 210,
   kSiteDecodeWaitEmpty = 211,
   kSiteDecodeWaitMerge = 212,
+  kSiteDecodeI8Context = 220,
+  kSiteDecodeI8Block = 221,
   kSitePrefillChunk = 300,
   kSitePrefillBlock = 301,
   kSitePrefillAlign = 302,

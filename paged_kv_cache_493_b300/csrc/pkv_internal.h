@@ -78,6 +78,50 @@ struct PrefillArgs {
   DeviceError* err;
 };
 
+// INT8 KV cache: codes int8 [num_blocks][256][Hkv][D], scales float32
+// [num_blocks][256][Hkv]; a code stands for code * scale.
+struct StoreI8Args {
+  const void* k;
+  const void* v;
+  int64_t k_row_stride;  // elements
+  int64_t v_row_stride;  // elements
+  const int32_t* slot_mapping;
+  int64_t num_tokens;
+  int8_t* k_codes;
+  int8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  int64_t num_blocks;
+  int num_kv_heads;
+  int head_dim;
+  DeviceError* err;
+};
+
+struct DecodeI8Args {
+  const void* q;
+  int64_t q_row_stride;  // elements
+  const int8_t* k_codes;
+  const int8_t* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* context_lens;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int64_t num_blocks;
+  float scale;
+  void* out;
+  int splits;   // token splits per (sequence, KV head): ceil(max_blocks * 256 / kInt8SplitTokens)
+  float* part;  // [num_seqs][num_kv_heads][splits][G][head_dim + 2]
+  DeviceError* err;
+};
+
+// Tokens per split of the INT8 decode.
+constexpr int kInt8SplitTokens = 512;
+
 // Tensor maps built by the API layer (cached per cache pointer).
 struct CacheMaps {
   CUtensorMap k_rows;   // decode: box {64, 1, 32} over [slots][Hkv][D], 128-byte swizzle
@@ -92,6 +136,12 @@ constexpr int kDecodeChunk = 32;
 constexpr int kPrefillKeyTile = 64;
 
 cudaError_t launch_store_kvcache(const StoreArgs& a, cudaStream_t stream);
+cudaError_t launch_store_kvcache_int8(const StoreI8Args& a, cudaStream_t stream);
+// Splits of the INT8 decode for a table width, and the bytes of its partials.
+int decode_int8_splits(int max_blocks);
+size_t decode_int8_partial_bytes(int64_t num_seqs, int num_kv_heads, int splits, int group,
+                                 int head_dim);
+cudaError_t launch_decode_int8(const DecodeI8Args& a, cudaStream_t stream);
 
 // Blocks of the decode kernel for a batch: as many as fit on the GPU at
 // once, at most num_pairs * max_splits when max_splits > 0.

@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -122,3 +122,38 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_missing_library_raises():
     with pytest.raises(pkv.PkvError):
         pkv.load_library("/nonexistent/libpkv.so")
+
+
+def test_int8_argument_validation(lib):
+    B = ctypes.c_void_p(0x1004)  # 4-byte aligned only
+
+    def store(**kw):
+        a = dict(k=A, v=A, ks=16 * 128, vs=16 * 128, sm=A, n=4, kc=A, vc=A, ksc=A, vsc=A, nb=8,
+                 hkv=16, d=128)
+        a.update(kw)
+        return lib.pkv_store_kvcache_int8(a["k"], a["v"], a["ks"], a["vs"], a["sm"], a["n"],
+                                          a["kc"], a["vc"], a["ksc"], a["vsc"], a["nb"],
+                                          a["hkv"], a["d"], NUL)
+
+    assert store(kc=NUL) == pkv.PKV_ERR_INVALID_ARG
+    assert store(vsc=NUL) == pkv.PKV_ERR_INVALID_ARG
+    assert store(nb=0) == pkv.PKV_ERR_INVALID_ARG
+    assert store(ks=100) == pkv.PKV_ERR_INVALID_ARG
+    assert store(d=96, ks=16 * 96, vs=16 * 96) == pkv.PKV_ERR_UNSUPPORTED
+    assert store(ksc=B) == pkv.PKV_ERR_UNSUPPORTED
+    assert store() == pkv.PKV_ERR_CUDA          # valid arguments, no device here
+
+    def dec8(**kw):
+        a = dict(q=A, qs=16 * 128, kc=A, vc=A, ksc=A, vsc=A, nb=8, bt=A, mb=2, cl=A, b=4, hq=16,
+                 hkv=8, d=128, scale=0.1, out=A)
+        a.update(kw)
+        return lib.pkv_decode_attention_int8(a["q"], a["qs"], a["kc"], a["vc"], a["ksc"],
+                                             a["vsc"], a["nb"], a["bt"], a["mb"], a["cl"], a["b"],
+                                             a["hq"], a["hkv"], a["d"], a["scale"], a["out"], NUL)
+
+    assert dec8(ksc=NUL) == pkv.PKV_ERR_INVALID_ARG
+    assert dec8(kc=NUL) == pkv.PKV_ERR_INVALID_ARG
+    assert dec8(hq=12, hkv=8) == pkv.PKV_ERR_INVALID_ARG
+    assert dec8(d=96, qs=16 * 96) == pkv.PKV_ERR_UNSUPPORTED
+    assert dec8(vsc=B) == pkv.PKV_ERR_UNSUPPORTED
+    assert dec8() == pkv.PKV_ERR_CUDA
