@@ -164,15 +164,18 @@ __global__ void __launch_bounds__(kI8Threads, G >= 8 ? 2 : 4) decode_int8_split_
       else
         bad = true;
     }
-    // Scores of this lane's token (log2 domain).
+    // Scores of this lane's token (log2 domain); its V scale, for P V.
     float sc[G];
+    float vs_mine = 0.f;
     if (slot >= 0) {
       const int8_t* krow = a.k_codes + (static_cast<int64_t>(slot) * hkv + kvh) * D;
       const float ks = a.k_scales[static_cast<int64_t>(slot) * hkv + kvh];
+      vs_mine = a.v_scales[static_cast<int64_t>(slot) * hkv + kvh];
       float dot[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) dot[g] = 0.f;
-#pragma unroll 2
+      constexpr int kKUnroll = (G <= 4 && D == 128) ? 4 : 2;  // 16-byte loads in flight per lane
+#pragma unroll kKUnroll
       for (int d0 = 0; d0 < D; d0 += 16) {
         const int4 raw = *reinterpret_cast<const int4*>(krow + d0);
         const int w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -202,11 +205,13 @@ __global__ void __launch_bounds__(kI8Threads, G >= 8 ? 2 : 4) decode_int8_split_
       m[g] = m_new;
     }
     // O += P V: lane owns dimensions lane * DPL .. lane * DPL + DPL - 1.
+    // Unrolled without branches so that several rows' loads are in flight;
+    // a token outside the context has weight 0 and reads the row of slot 0.
+#pragma unroll 8
     for (int j = 0; j < 32; ++j) {
       const int sj = __shfl_sync(0xffffffffu, slot, j);
-      if (sj < 0) continue;  // the same for every lane
-      const int64_t r = static_cast<int64_t>(sj) * hkv + kvh;
-      const float vs = a.v_scales[r];
+      const float vs = __shfl_sync(0xffffffffu, vs_mine, j);
+      const int64_t r = static_cast<int64_t>(sj < 0 ? 0 : sj) * hkv + kvh;
       const int8_t* vrow = a.v_codes + r * D + lane * DPL;
       float vf[DPL];
       if constexpr (DPL == 4) {
