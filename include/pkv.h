@@ -283,8 +283,9 @@ pkv_status pkv_set_max_splits(int32_t max_splits);
 
 /*
  * Allocate, on the current device, the decode workspace for batches up to
- * the given shape, so that later calls of that size or smaller never
- * allocate (required before stream capture).  Grows, never shrinks.
+ * the given shape (pkv_decode_attention and pkv_decode_attention_int8), so
+ * that later calls of that size or smaller never allocate (required before
+ * stream capture).  Grows, never shrinks.
  */
 pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_blocks_per_seq);

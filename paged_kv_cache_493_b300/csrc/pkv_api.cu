@@ -531,9 +531,12 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
     const int64_t pairs = static_cast<int64_t>(num_seqs) * (num_q_heads / g);
     const int ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
     part = std::max(part, pkv::decode_partial_bytes(ctas, g, head_dim));
+    // The INT8 decode keeps its split partials in the same workspace.
+    part = std::max(part, pkv::decode_int8_partial_bytes(num_seqs, num_q_heads / g,
+                                                         pkv::decode_int8_splits(max_blocks_per_seq),
+                                                         g, head_dim));
     cnt = std::max(cnt, pkv::decode_counter_bytes(pairs));
   }
-  (void)max_blocks_per_seq;
   return ensure_workspace(ds, part, cnt);
 }
 
