@@ -518,8 +518,9 @@ def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
 def host_block_manager(pkv, steps: int = 2000) -> dict:
     """Host cost of producing the decode inputs: the block manager (C++, behind
     the C ABI) admitting 128 prompts of 4096 tokens that share a 2048-token
-    prefix, then decode steps that append one token to each of the 128
-    sequences and fill the [128, max_blocks] block table and context lengths."""
+    prefix, then decode steps (one call each) that append one token to each of
+    the 128 sequences and fill the slot mapping, the [128, max_blocks] block
+    table and the context lengths."""
     prompts = W.shared_prefix_prompts()
     b = len(prompts)
     max_blocks = -(-(4096 + steps) // W.BLOCK_SIZE)
@@ -535,8 +536,7 @@ def host_block_manager(pkv, steps: int = 2000) -> dict:
     t0 = time.perf_counter()
     for i in range(steps):
         tokens.fill_(i)
-        bm.append_decode_into(ids, tokens, slots)
-        bm.block_tables_into(ids, tables, lens)
+        bm.decode_step_into(ids, tokens, slots, tables, lens)
     step_s = (time.perf_counter() - t0) / steps
     ok = bool((lens == 4096 + steps).all()) and bm.num_free_blocks() == 8 * 1024 - (
         2048 // W.BLOCK_SIZE + b * (-(-(4096 + steps) // W.BLOCK_SIZE) - 2048 // W.BLOCK_SIZE))

@@ -384,6 +384,15 @@ pkv_status pkv_bm_append(pkv_block_manager* bm, int64_t seq_id, const int32_t* t
 pkv_status pkv_bm_append_decode(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs,
                                 const int32_t* tokens, int32_t* slot_mapping);
 
+/* One decode step in one call: pkv_bm_append_decode, then the step's
+ * block_tables [num_seqs][max_blocks] and context_lens [num_seqs] as
+ * pkv_bm_block_tables gives them.  Fails as a whole, changing nothing:
+ * PKV_ERR_INVALID_ARG for an unknown or repeated id or a table that would
+ * outgrow max_blocks, PKV_ERR_NO_MEMORY when too few blocks are free. */
+pkv_status pkv_bm_decode_step(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs,
+                              const int32_t* tokens, int32_t max_blocks, int32_t* slot_mapping,
+                              int32_t* block_tables, int32_t* context_lens);
+
 /* Drop sequence seq_id: every block of its table loses one count. */
 pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
 

@@ -128,6 +128,19 @@ class BlockManagerModel:
             raise BlockManagerError("no_memory")
         return [self.append(s, [tok])[0] for s, tok in zip(seq_ids, tokens)]
 
+    def decode_step(self, seq_ids, tokens, max_blocks: int):
+        """append_decode, then the step's tables; nothing changes on failure."""
+        seq_ids = list(seq_ids)
+        if len(set(seq_ids)) != len(seq_ids):
+            raise BlockManagerError("invalid", "repeated sequence")
+        for s in seq_ids:
+            q = self._seq(s)
+            if len(q["table"]) + (1 if len(q["tokens"]) % BLOCK == 0 else 0) > max_blocks:
+                raise BlockManagerError("invalid", "table would outgrow max_blocks")
+        slots = self.append_decode(seq_ids, tokens)
+        rows, lens = self.block_tables(seq_ids, max_blocks)
+        return slots, rows, lens
+
     def free_seq(self, seq_id: int) -> None:
         seq = self._seq(seq_id)
         for b in reversed(seq["table"]):

@@ -58,6 +58,7 @@ SIGNATURES = {
     "pkv_bm_allocate": ([_P, _I64, _P, _I32, ctypes.POINTER(_I32)], _I32),
     "pkv_bm_append": ([_P, _I64, _P, _I32, _P], _I32),
     "pkv_bm_append_decode": ([_P, _P, _I32, _P, _P], _I32),
+    "pkv_bm_decode_step": ([_P, _P, _I32, _P, _I32, _P, _P, _P], _I32),
     "pkv_bm_free": ([_P, _I64], _I32),
     "pkv_bm_block_tables": ([_P, _P, _I32, _I32, _P, _P], _I32),
     "pkv_bm_slots": ([_P, _I64, _I32, _I32, _P], _I32),
@@ -386,6 +387,39 @@ class BlockManager:
         _check(self._lib.pkv_bm_append_decode(self._h, _ptr(seq_ids), seq_ids.numel(),
                                               _ptr(tokens), _ptr(slot_mapping)),
                "pkv_bm_append_decode")
+
+    def decode_step(self, seq_ids, tokens, max_blocks: int):
+        """One decode step: (slot_mapping, block_tables rows, context_lens) as lists."""
+        seq_ids = [int(x) for x in seq_ids]
+        buf, n = _host_i32(tokens)
+        _need(n == len(seq_ids), "decode_step: one token per sequence")
+        mb = int(max_blocks)
+        ids = (ctypes.c_int64 * max(n, 1))(*seq_ids)
+        slots = (ctypes.c_int32 * max(n, 1))()
+        tables = (ctypes.c_int32 * max(n * mb, 1))()
+        lens = (ctypes.c_int32 * max(n, 1))()
+        _check(self._lib.pkv_bm_decode_step(self._h, ids, n, buf, mb, slots, tables, lens),
+               "pkv_bm_decode_step")
+        return list(slots[:n]), [list(tables[i * mb:(i + 1) * mb]) for i in range(n)], list(lens[:n])
+
+    def decode_step_into(self, seq_ids, tokens, slot_mapping, block_tables, context_lens) -> None:
+        """decode_step on CPU tensors (pinned ones can be copied to the device
+        asynchronously): seq_ids int64 [B], tokens int32 [B]; fills int32
+        slot_mapping [B], block_tables [B, max_blocks] and context_lens [B]."""
+        import torch
+        b = seq_ids.numel()
+        for t, dt, name in ((seq_ids, torch.int64, "seq_ids"), (tokens, torch.int32, "tokens"),
+                            (slot_mapping, torch.int32, "slot_mapping"),
+                            (context_lens, torch.int32, "context_lens")):
+            _need(t.device.type == "cpu" and t.dtype == dt and t.is_contiguous() and t.numel() == b,
+                  f"{name}: contiguous CPU {dt} [B]")
+        _need(block_tables.device.type == "cpu" and block_tables.dtype == torch.int32
+              and block_tables.is_contiguous() and block_tables.dim() == 2
+              and block_tables.shape[0] == b, "block_tables: CPU int32 [B, max_blocks]")
+        _check(self._lib.pkv_bm_decode_step(self._h, _ptr(seq_ids), b, _ptr(tokens),
+                                            block_tables.shape[1], _ptr(slot_mapping),
+                                            _ptr(block_tables), _ptr(context_lens)),
+               "pkv_bm_decode_step")
 
     def free(self, seq_id: int) -> None:
         _check(self._lib.pkv_bm_free(self._h, int(seq_id)), "pkv_bm_free")

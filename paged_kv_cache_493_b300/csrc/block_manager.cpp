@@ -319,6 +319,53 @@ pkv_status pkv_bm_append_decode(pkv_block_manager* bm, const int64_t* seq_ids, i
   return PKV_OK;
 }
 
+pkv_status pkv_bm_decode_step(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs,
+                              const int32_t* tokens, int32_t max_blocks, int32_t* slot_mapping,
+                              int32_t* block_tables, int32_t* context_lens) {
+  if (!bm || num_seqs < 0 || max_blocks < 0) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!seq_ids || !tokens || !slot_mapping || !context_lens || (max_blocks > 0 && !block_tables))
+    return PKV_ERR_INVALID_ARG;
+  try {
+    // Everything is checked before anything changes: known, distinct ids,
+    // tables that still fit max_blocks after the token, enough free blocks.
+    bm->batch.resize(num_seqs);
+    const uint64_t stamp = ++bm->calls;
+    int64_t need = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      auto it = bm->seqs.find(seq_ids[s]);
+      if (it == bm->seqs.end() || it->second.stamp == stamp ||
+          it->second.num_tokens == INT32_MAX)
+        return PKV_ERR_INVALID_ARG;
+      Sequence& seq = it->second;
+      seq.stamp = stamp;
+      bm->batch[s] = &seq;
+      const bool opens = seq.num_tokens % kTokensPerBlock == 0;
+      if (static_cast<int64_t>(seq.table.size()) + (opens ? 1 : 0) > max_blocks)
+        return PKV_ERR_INVALID_ARG;
+      need += opens ? 1 : 0;
+    }
+    if (need > static_cast<int64_t>(bm->free_list.size())) return PKV_ERR_NO_MEMORY;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      Sequence& seq = *bm->batch[s];
+      if (seq.num_tokens % kTokensPerBlock == 0) seq.table.reserve(seq.table.size() + 1);
+      seq.tail.reserve(kTokensPerBlock);
+    }
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      Sequence& seq = *bm->batch[s];
+      slot_mapping[s] = bm->append_one(seq, tokens[s]);
+      const int32_t used = static_cast<int32_t>(seq.table.size());
+      int32_t* row = block_tables + static_cast<int64_t>(s) * max_blocks;
+      std::memcpy(row, seq.table.data(), sizeof(int32_t) * used);
+      for (int32_t i = used; i < max_blocks; ++i) row[i] = -1;
+      context_lens[s] = seq.num_tokens;
+    }
+  } catch (...) {
+    return PKV_ERR_NO_MEMORY;
+  }
+  return PKV_OK;
+}
+
 pkv_status pkv_bm_free(pkv_block_manager* bm, int64_t seq_id) {
   if (!bm) return PKV_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq_id);

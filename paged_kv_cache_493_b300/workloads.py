@@ -265,6 +265,7 @@ def block_manager_trace(seed: int, num_ops: int, num_prefixes: int = 4, vocab: i
       ("free", seq_id)               ("slots", seq_id, begin, end)
       ("tables", [seq_id, ...], max_blocks)
       ("decode", [seq_id, ...], tokens)   (one token for each sequence)
+      ("step", [seq_id, ...], tokens, max_blocks)   (the same, with the step's tables)
 
     A small share of ops is invalid on purpose (unknown or repeated sequence
     ids, a token range past the end, a table narrower than a sequence, a
@@ -325,7 +326,11 @@ def block_manager_trace(seed: int, num_ops: int, num_prefixes: int = 4, vocab: i
         elif r < 0.85:
             ids = [s for s in torch.randperm(len(live), generator=g).tolist()]
             ids = [list(live)[i] for i in ids[:randint(1, len(live))]]
-            ops.append(("decode", ids, tokens(len(ids))))
+            if randint(0, 1):
+                ops.append(("decode", ids, tokens(len(ids))))
+            else:  # a table width that sometimes cannot hold the step
+                width = max(-(-(live[s] + 1) // BLOCK_SIZE) for s in ids) + randint(-1, 1)
+                ops.append(("step", ids, tokens(len(ids)), max(width, 0)))
             for s in ids:
                 live[s] += 1
         elif r < 0.93:

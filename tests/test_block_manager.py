@@ -51,6 +51,9 @@ class Lib:
     def append_decode(self, ids, tokens):
         return self._call(self.bm.append_decode, ids, tokens)
 
+    def decode_step(self, ids, tokens, max_blocks):
+        return self._call(self.bm.decode_step, ids, tokens, max_blocks)
+
     def free_seq(self, s):
         return self._call(self.bm.free, s)
 
@@ -312,6 +315,25 @@ def test_decode_step_that_does_not_fit_changes_nothing(make):
     assert bm.append_decode([2], [9]) == [2 * BLOCK + 5]
 
 
+def test_decode_step_gives_slots_tables_and_lengths(make):
+    bm = make(3)
+    bm.allocate(0, toks(36, BLOCK))              # block 0, full
+    bm.allocate(1, toks(37, 10))                 # block 1
+    assert bm.decode_step([1, 0], [5, 6], 2) == ([BLOCK + 10, 2 * BLOCK], [[1, -1], [0, 2]],
+                                                  [11, BLOCK + 1])
+
+
+def test_decode_step_that_outgrows_the_table_changes_nothing(make):
+    bm = make(3)
+    bm.allocate(0, toks(38, BLOCK))              # a full block: the next token opens another
+    bm.allocate(1, toks(39, 3))
+    with pytest.raises(BlockManagerError) as e:
+        bm.decode_step([1, 0], [1, 2], 1)
+    assert e.value.kind == "invalid"
+    assert bm.block_tables([0, 1], 1) == ([[0], [1]], [BLOCK, 3])
+    assert bm.num_free_blocks() == 1
+
+
 def test_invalid_calls_raise_and_change_nothing(make):
     bm = make(4)
     bm.allocate(0, toks(30, 300))
@@ -339,7 +361,7 @@ def test_every_sequence_reads_its_own_prefix(make, seed):
                 sim.append(bm, op[1], op[2])
             elif op[0] == "free" and op[1] in sim.tokens:
                 sim.free(bm, op[1])
-            elif op[0] == "decode" and all(x in sim.tokens for x in op[1]):
+            elif op[0] in ("decode", "step") and all(x in sim.tokens for x in op[1]):
                 sim.append_decode(bm, op[1], op[2])
         except BlockManagerError as e:
             assert e.kind == "no_memory"
@@ -363,6 +385,8 @@ def run_op(bm, op):
             return bm.slots(op[1], op[2], op[3])
         if op[0] == "decode":
             return bm.append_decode(op[1], op[2])
+        if op[0] == "step":
+            return bm.decode_step(op[1], op[2], op[3])
         return bm.block_tables(op[1], op[2])
     except BlockManagerError as e:
         return ("error", e.kind)
@@ -388,7 +412,7 @@ def test_library_matches_model_call_by_call(seed, num_blocks, num_ops, max_live)
         width = max([len(model.seqs[s]["table"]) for s in live] + [0])
         assert lib.block_tables(sorted(live), width) == model.block_tables(sorted(live), width), i
     assert {("error", "invalid"), ("error", "no_memory"), "allocate", "append", "free", "slots",
-            "tables", "decode"} <= outcomes
+            "tables", "decode", "step"} <= outcomes
 
 
 def test_block_tables_into_fills_host_tensors():
@@ -495,6 +519,8 @@ MUTANTS = {
     "free_check_ignores_table": ("- len(table) > len(self.free)", "> len(self.free)"),
     "decode_counts_every_sequence": ('len(q["tokens"]) % BLOCK == 0)', 'len(q["tokens"]) % BLOCK >= 0)'),
     "decode_allows_repeats": ("or len(set(seq_ids)) != len(seq_ids)", ""),
+    "step_width_off_by_one": ("if len(q[\"table\"]) + (1 if len(q[\"tokens\"]) % BLOCK == 0 else 0) > max_blocks:",
+                              "if len(q[\"table\"]) > max_blocks:"),
 }
 
 PIN_TESTS = [
@@ -512,6 +538,8 @@ PIN_TESTS = [
     test_invalid_calls_raise_and_change_nothing,
     test_decode_step_appends_one_token_per_sequence,
     test_decode_step_that_does_not_fit_changes_nothing,
+    test_decode_step_gives_slots_tables_and_lengths,
+    test_decode_step_that_outgrows_the_table_changes_nothing,
     lambda make: test_every_sequence_reads_its_own_prefix(make, 0),
     lambda make: test_every_sequence_reads_its_own_prefix(make, 1),
 ]
