@@ -104,7 +104,7 @@ def test_int8_qwen_decode_b128(cuda_device):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (32, 2), (16, 1)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 4), (64, 8), (32, 2), (16, 1)])
 def test_int8_geometries(cuda_device, d, hq, hkv):
     case = W.make_decode_case("g8", [0, 1, 300, 1100, 513], hq, hkv, d, 24, seed=hq * 7 + hkv + d)
     check_case(case)
