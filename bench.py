@@ -51,11 +51,33 @@ from paged_kv_cache_493_b300 import workloads as W  # noqa: E402
 METRIC = "paged decode attention KV GB/s (% of HBM peak) and decode tokens/s/layer"
 MAIN_WORKLOAD = "qwen_decode_b128"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-# DRAM bytes (read + write) of one decode_split launch on qwen_decode_b128,
-# from the ncu capture summarised in profiles/decode_split_qwen_decode_b128.md.
-# Valid only for the kernel version that capture measured: set to None when
-# the kernel changes, until it is captured again.
-DECODE_SPLIT_TRAFFIC_BYTES = 328.3e6
+# DRAM bytes (read + write) of one launch of a kernel on a workload, from an
+# ncu capture, keyed by the SHA-256 of the kernel's source files at the time
+# of the capture: the figure is reported only while the sources still hash to
+# that value (any change to the kernel makes it null until captured again).
+KERNEL_SOURCES = {
+    "decode_split": ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h"),
+}
+TRAFFIC_CAPTURES = {
+    # kernel: (sha256 of its sources, workload, dram bytes per launch)
+    "decode_split": (None, MAIN_WORKLOAD, None),
+}
+
+
+def sources_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "paged_kv_cache_493_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel: str, workload: str):
+    digest, wl, dram = TRAFFIC_CAPTURES.get(kernel, (None, None, None))
+    if digest is None or wl != workload or dram is None:
+        return None
+    return dram if sources_digest(kernel) == digest else None
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -102,11 +124,11 @@ def decode_step_bytes(case) -> dict:
     """Algorithmic bytes of one decode step: every cached K/V row read once, q
     read, out written, new rows read and written, metadata read."""
     kv = decode_kv_bytes(case)
-    q = case.q.numel() * 2
+    q = case.q.numel() * 2  # q read; the bf16 output written is the same size
     new = (case.k_new.numel() + case.v_new.numel()) * 2
     meta = (case.cache.block_tables.numel() + case.cache.context_lens.numel() +
             case.slot_mapping.numel()) * 4
-    return {"kv": kv, "split_kernel": kv + q + meta, "step": kv + 2 * q + 2 * new + meta}
+    return {"kv": kv, "split_kernel": kv + 2 * q + meta, "step": kv + 2 * q + 2 * new + meta}
 
 
 def unique_kv_bytes(case) -> int:
@@ -262,24 +284,61 @@ class DecodeBench:
         p.pkv_decode_attention(self.q, self.kc, self.vc, self.bt, self.cl, self.case.scale, self.out)
 
     def e2e_setup(self):
+        """A step's inputs (q, new K/V rows, slot mapping, block tables,
+        context lengths) packed into one pinned host buffer and one device
+        buffer of the same layout (each tensor at a 256-byte-aligned offset),
+        so a step makes one host-to-device copy and one device-to-host copy
+        of the output."""
         c = self.case
-        pin = lambda t: t.clone().pin_memory()  # noqa: E731
-        self.h_in = [pin(c.q), pin(c.k_new), pin(c.v_new), pin(c.slot_mapping),
-                     pin(c.cache.block_tables), pin(c.cache.context_lens)]
-        self.d_in = [torch.empty_like(t, device="cuda") for t in self.h_in]
+        srcs = [c.q, c.k_new, c.v_new, c.slot_mapping, c.cache.block_tables, c.cache.context_lens]
+        offs, total = [], 0
+        for t in srcs:
+            offs.append(total)
+            total += -(-t.numel() * t.element_size() // 256) * 256
+        self.h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.d_buf = torch.empty(total, dtype=torch.uint8, device="cuda")
+
+        def view(buf, off, t):
+            n = t.numel() * t.element_size()
+            return buf[off:off + n].view(t.dtype).view(t.shape)
+
+        for t, off in zip(srcs, offs):
+            view(self.h_buf, off, t).copy_(t)
+        self.d_in = [view(self.d_buf, off, t) for t, off in zip(srcs, offs)]
         self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in self.h_in)
-        d2h = self.h_out.numel() * self.h_out.element_size()
-        return h2d, d2h
+        return total, self.h_out.numel() * self.h_out.element_size()
 
     def e2e_step(self):
         p = self.pkv
-        for h, d in zip(self.h_in, self.d_in):
-            d.copy_(h, non_blocking=True)
+        self.d_buf.copy_(self.h_buf, non_blocking=True)
         q, kn, vn, sm, bt, cl = self.d_in
         p.pkv_store_kvcache(kn, vn, sm, self.kc, self.vc)
         p.pkv_decode_attention(q, self.kc, self.vc, bt, cl, self.case.scale, self.out)
         self.h_out.copy_(self.out, non_blocking=True)
+
+    def e2e_phases(self, steps: int, flush) -> dict:
+        """Per-phase device time of the eager end-to-end step (CUDA events on
+        the stream): input copy, the two library calls, output copy."""
+        stream = torch.cuda.current_stream()
+        tot = {"h2d": 0.0, "calls": 0.0, "d2h": 0.0}
+        p = self.pkv
+        for _ in range(steps):
+            flush()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            self.d_buf.copy_(self.h_buf, non_blocking=True)
+            ev[1].record(stream)
+            q, kn, vn, sm, bt, cl = self.d_in
+            p.pkv_store_kvcache(kn, vn, sm, self.kc, self.vc)
+            p.pkv_decode_attention(q, self.kc, self.vc, bt, cl, self.case.scale, self.out)
+            ev[2].record(stream)
+            self.h_out.copy_(self.out, non_blocking=True)
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            tot["h2d"] += ev[0].elapsed_time(ev[1])
+            tot["calls"] += ev[1].elapsed_time(ev[2])
+            tot["d2h"] += ev[2].elapsed_time(ev[3])
+        return {k + "_ms": round(v / steps, 5) for k, v in tot.items()}
 
 
 def capture_graph(step):
@@ -342,12 +401,21 @@ def run_gpu(args, rank, world, local):
     achieved = bytes_["split_kernel"] / (split_ms * 1e-3) / 1e9
     launches_per_step = sum(n for _, n in kt.values()) / args.steps
 
-    # End to end through the C ABI from pinned host buffers.
+    # End to end through the C ABI from pinned host buffers: one packed
+    # host-to-device copy of the step's inputs, the two calls, the output
+    # copied back; timed as a captured graph (how an engine replays its decode
+    # step, copies included) and eagerly (one Python call per operation).
     h2d, d2h = bench.e2e_setup()
     for _ in range(args.warmup):
         bench.e2e_step()
-    e2e_per, _ = time_steps(bench.e2e_step, args.steps, flush)
+    e2e_eager_per, _ = time_steps(bench.e2e_step, args.steps, flush)
+    e2e_replay = capture_graph(bench.e2e_step)
+    for _ in range(args.warmup):
+        e2e_replay()
+    e2e_per, _ = time_steps(e2e_replay, args.steps, flush)
     e2e_ms = reduce_max(sum(e2e_per) / len(e2e_per))
+    e2e_eager_ms = reduce_max(sum(e2e_eager_per) / len(e2e_eager_per))
+    phases = bench.e2e_phases(args.steps, flush)
     torch.cuda.synchronize()
     e2e_ok = torch.equal(bench.h_out.to("cuda"), bench.out)
 
@@ -391,14 +459,20 @@ def run_gpu(args, rank, world, local):
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": DECODE_SPLIT_TRAFFIC_BYTES,
+            "traffic": captured_traffic("decode_split", MAIN_WORKLOAD),
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, "
+                              "valid only for the kernel sources it was captured on",
             "algorithmic_bytes_per_launch": bytes_["split_kernel"],
             "avg_launch_ms": round(split_ms, 5),
             "kernel_ms": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},
         },
         "e2e": {"value": round(world * bytes_["step"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "output_matches_device": bool(e2e_ok)},
+                "d2h_bytes_per_step": d2h, "output_matches_device": bool(e2e_ok),
+                "how": "one packed pinned H2D copy + pkv_store_kvcache + pkv_decode_attention "
+                       "+ pinned D2H of out, captured once as a CUDA graph and replayed",
+                "eager_ms_per_step": round(e2e_eager_ms, 5),
+                "eager_phases": phases},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clk.summary(2032.0),
         "device_error": code,
@@ -574,37 +648,64 @@ def oracle_step_sample(case, seqs):
     return int(c.context_lens[sel].sum()) * hkv * d * 4
 
 
-def cpu_baseline(case, bytes_, budget_s: float = 15.0):
-    """The oracle as it stands (single thread, fp64) on a bounded sample."""
+def oracle_step_parallel(case, seqs, workers):
+    """store + decode of the listed sequences on the CPU oracle over `workers`
+    host threads (oracle.parallel: the same C functions, one task per
+    sequence); returns KV bytes processed."""
+    import oracle
+    import oracle.parallel as op
+    c = case.cache
+    sel = torch.tensor(seqs, dtype=torch.long)
+    kc, vc = oracle.store_kvcache(case.k_new[sel], case.v_new[sel], case.slot_mapping[sel],
+                                  c.k_cache, c.v_cache)
+    op.decode(case.q[sel], kc, vc, c.block_tables[sel], c.context_lens[sel], case.scale,
+              workers=workers)
+    hkv, d = int(c.k_cache.shape[2]), int(c.k_cache.shape[3])
+    return int(c.context_lens[sel].sum()) * hkv * d * 4
+
+
+def cpu_baseline(case, bytes_, budget_s: float = 12.0):
+    """The oracle as it stands (fp64 C) on a bounded sample of the workload:
+    single-threaded, and over every host core (one task per sequence)."""
+    import oracle.parallel as op
     n = case.num_seqs
-    seqs, done, elapsed = [], 0, 0.0
-    order = list(range(n))
-    t0 = time.perf_counter()
-    kv = 0
-    i = 0
-    while i < n and time.perf_counter() - t0 < budget_s:
-        chunk = order[i:i + 16]
-        kv += oracle_step_sample(case, chunk)
-        i += len(chunk)
-    elapsed = time.perf_counter() - t0
-    return {"value": round(kv / elapsed / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"store + decode of {i} of {n} sequences (all heads), {elapsed:.1f} s, "
-                      f"fp64 single-threaded C"}
+    cores = op.host_cores()
+
+    def leg(workers, batch):
+        t0 = time.perf_counter()
+        kv, i = 0, 0
+        while i < n and time.perf_counter() - t0 < budget_s:
+            chunk = list(range(i, min(n, i + batch)))
+            kv += (oracle_step_sample(case, chunk) if workers == 1
+                   else oracle_step_parallel(case, chunk, workers))
+            i += len(chunk)
+        return kv / (time.perf_counter() - t0) / 1e9, i, time.perf_counter() - t0
+
+    one, n1, t1 = leg(1, 16)
+    many, nm, tm = leg(cores, max(cores, 16))
+    return {"value": round(many, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "host_cpu_count": os.cpu_count(),
+            "sample": f"store + decode of {nm} of {n} sequences (all heads), {tm:.1f} s, fp64 C "
+                      f"over {cores} threads (one sequence per task)",
+            "single_core": {"value": round(one, 6), "cores": 1,
+                            "sample": f"store + decode of {n1} of {n} sequences, {t1:.1f} s"}}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    import oracle.parallel as op
     case = W.qwen_decode(seed=1002)
-    per_step = 8  # sequences per step: a bounded sample of the workload
+    cores = op.host_cores()
+    per_step = min(case.num_seqs, max(8, cores))  # sequences per step: a bounded sample
     n = case.num_seqs
     for i in range(args.warmup):
-        oracle_step_sample(case, [(i * per_step + j) % n for j in range(per_step)])
+        oracle_step_parallel(case, [(i * per_step + j) % n for j in range(per_step)], cores)
     times, kv = [], 0
     for i in range(args.steps):
         seqs = [(i * per_step + j) % n for j in range(per_step)]
         t0 = time.perf_counter()
-        kv += oracle_step_sample(case, seqs)
+        kv += oracle_step_parallel(case, seqs, cores)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = kv / total / 1e9
@@ -617,8 +718,10 @@ def run_reference(args, rank, world):
         "config": {"workload": MAIN_WORKLOAD, "num_seqs": n, "num_q_heads": 16, "num_kv_heads": 8,
                    "head_dim": 128, "block_size": 256, "num_blocks": case.cache.num_blocks,
                    "parallelism": "host cores"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"each step: store + decode of {per_step} of {n} sequences"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "host_cpu_count": os.cpu_count(),
+                         "sample": f"each step: store + decode of {per_step} of {n} sequences, "
+                                   f"fp64 C over {cores} threads (one sequence per task)"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -639,7 +742,22 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "pkv":
         args.warmup = 3
+    if args.gpus > 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        # N replicas need one process per GPU: start them under torchrun.
+        if args.impl == "pkv" and torch.cuda.device_count() < args.gpus:
+            sys.exit(f"--gpus {args.gpus}: only {torch.cuda.device_count()} CUDA device(s) visible")
+        import socket
+        with socket.socket() as s:
+            s.bind(("127.0.0.1", 0))
+            port = s.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr=127.0.0.1",
+               f"--master-port={port}", os.path.abspath(__file__)] + list(
+                   argv if argv is not None else sys.argv[1:])
+        sys.exit(subprocess.call(cmd))
     rank, world, local = dist_setup()
+    if world != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one process per GPU")
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)

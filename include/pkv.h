@@ -164,11 +164,11 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
 /*
  * pkv_decode_attention_noalloc -- pkv_decode_attention for callers that
  * cannot let the library allocate device memory: serving engines that hand
- * nearly all free memory to the KV block pool at start-up, code running
- * while a stream is captured into a CUDA graph (where cudaMalloc is not
- * allowed), and processes whose device memory must all come from one
- * caching allocator.  The pages describe no such variant; it is an
- * addition of this library.
+ * nearly all free memory to the KV block pool at start-up (a workspace the
+ * library allocated later could fail, or escape the engine's accounting),
+ * and processes whose device memory must all come from one caching
+ * allocator.  The pages describe no such variant; it is an addition of this
+ * library.
  *
  * Arguments, layouts, results and the split plan are those of
  * pkv_decode_attention.  The difference is where the split-K partials go:
@@ -177,28 +177,29 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
  * workspace.  The call itself calls no cudaMalloc, cudaFree or allocating
  * library routine.
  *
- * - Size limit: the array holds a 256-byte error word, a 2 MiB region of
- *   arrival counters (8 bytes per (sequence, KV head) pair, so at most
- *   262144 pairs: num_seqs * num_kv_heads <= 262144) and the partials,
+ * - Size limit: the array holds a 2 MiB region of arrival counters (8 bytes
+ *   per (sequence, KV head) pair after a 256-byte header, so at most 262144
+ *   pairs: num_seqs * num_kv_heads <= 262144) and the partials,
  *   2 * B * G * (head_dim + 2) * 4 bytes, where G = num_q_heads /
  *   num_kv_heads and B is the decode kernel's grid (the blocks that fit on
  *   the GPU at once, a few per SM; at most num_seqs * num_kv_heads * cap
  *   under pkv_set_max_splits(cap)), which must fit in the remaining
- *   14 MiB - 256 bytes (a few MB on a 148-SM B300).  A
- *   batch beyond either limit returns PKV_ERR_UNSUPPORTED and launches
- *   nothing.
+ *   14 MiB - 256 bytes (a few MB on a 148-SM B300).  A batch beyond either
+ *   limit returns PKV_ERR_UNSUPPORTED and launches nothing.
  * - Set-up: the first call on each device, with that device current, looks
  *   up the array's device address (cudaGetSymbolAddress); make that first
- *   call before any stream capture.
+ *   call before any stream capture.  A failed lookup is retried by the next
+ *   call.
  * - Sharing: every call on a device uses the same array, which keeps the
  *   last call's contents.  Nothing needs clearing: the kernel writes every
  *   partial it reads, and its arrival counters (zero at load) carry the
  *   number of the call that wrote them, so older values count as zero.
  *   Calls whose kernels overlap on the GPU (on different streams without
  *   ordering) race on it: serialise them.
- * - Device-side checks still zero the output rows of out-of-range block ids
- *   or lengths, but their error code goes to a word inside the array and is
- *   not reported by pkv_get_device_error.
+ * - Device-side checks zero the output rows of out-of-range block ids or
+ *   lengths and record PKV_ERR_DEVICE_CHECK (or PKV_ERR_TIMEOUT) in the
+ *   library's error word, a static device variable too: pkv_get_device_error
+ *   reports it as for every other call.
  */
 pkv_status pkv_decode_attention_noalloc(const void* q, int64_t q_row_stride, const void* k_cache,
                                         const void* v_cache, int64_t num_blocks,
@@ -264,7 +265,8 @@ pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const 
 
 /*
  * Synchronise `stream`, then read and clear the current device's error
- * word.  *code receives PKV_OK or the first PKV_ERR_DEVICE_CHECK /
+ * word (a static device variable of the library, shared by every call on
+ * that device; reading it allocates nothing).  *code receives PKV_OK or the first PKV_ERR_DEVICE_CHECK /
  * PKV_ERR_TIMEOUT recorded since the last read; *info (may be NULL) an
  * internal site code for diagnostics.  Returns PKV_ERR_CUDA if the
  * synchronisation failed.

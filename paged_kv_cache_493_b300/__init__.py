@@ -174,9 +174,11 @@ def pkv_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens
                                  out, stream=None) -> None:
     """pkv_decode_attention with its split-K scratch in the library's static
     16 MiB device array: the call allocates no device memory, for callers that
-    cannot allocate (a KV pool that already holds the free memory, stream
-    capture).  Raises PkvError(PKV_ERR_UNSUPPORTED) for a batch whose partials
-    do not fit; overlapping calls on one device race on the shared array."""
+    cannot allocate (a KV pool that already holds the free memory, a process
+    whose memory all comes from one caching allocator).  Raises
+    PkvError(PKV_ERR_UNSUPPORTED) for a batch whose partials do not fit;
+    overlapping calls on one device race on the shared array.  Device-side
+    check failures are read with pkv_get_device_error, as for every call."""
     nb, hkv, d = _cache(k_cache, v_cache)
     _need(q.dim() == 3, "q: [B, Hq, D]")
     b, hq = int(q.shape[0]), int(q.shape[1])

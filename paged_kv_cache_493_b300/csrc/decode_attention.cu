@@ -137,6 +137,60 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 
 constexpr int kPanelBytes = kDecodeChunk * 128;  // 32 rows x 64 dimensions (bf16)
 
+// Scratch of one warp folding the shared-prefix partials of a pair into the
+// state of its private part (cascade decode).
+template <int G>
+struct FoldScratch {
+  float fp[G];     // factor of the private state, 2^(M_private - M)
+  float L[G];      // merged sum
+  int bad[G];      // a unit's row failed
+  float w[G][kMaxSharedUnits];  // factor of unit u, 2^(m_u - M)
+};
+
+// Cascade decode, one head h of pair (seq, kvh), by one warp: given the
+// private part's reference max Mp and sum Lp, reads the shared_units partial
+// states (m_u, l_u) of the row and computes the merged reference
+// M = max(Mp, max_u m_u), the factors fp = 2^(Mp - M) and w_u = 2^(m_u - M),
+// and L = Lp fp + sum_u l_u w_u (log-sum-exp merge, as for split pieces).
+// Lane u handles unit u (shared_units <= 32).  Results go to f (lane 0
+// writes fp, L, bad; lane u writes w[h][u]); the caller syncs the warp.
+template <int G>
+__device__ __forceinline__ void fold_head(const DecodeArgs& a, int seq, int kvh, int h, float Mp,
+                                          float Lp, FoldScratch<G>& f, int lane) {
+  const int U = a.shared_units;
+  const int64_t row = (static_cast<int64_t>(kvh) * U + lane) * a.shared_rows_pad +
+                      static_cast<int64_t>(seq) * G + h;
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < U) ml = __ldcg(reinterpret_cast<const float2*>(a.shared_ml) + row);
+  const bool bad = __any_sync(0xffffffffu, lane < U && ml.y < 0.f);
+  float M = ml.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  M = fmaxf(M, Mp);
+  const bool none = M == -INFINITY;
+  const float w = (lane < U && !none && ml.x != -INFINITY) ? fast_exp2(ml.x - M) : 0.f;
+  float Ls = ml.y * w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  if (lane < U) f.w[h][lane] = w;
+  if (lane == 0) {
+    const float fp = (none || Mp == -INFINITY) ? 0.f : fast_exp2(Mp - M);
+    f.fp[h] = fp;
+    f.L[h] = Lp * fp + Ls;
+    f.bad[h] = bad ? 1 : 0;
+  }
+}
+
+// Address of dimension d of head h's unnormalised output in unit u's partial
+// state of pair (seq, kvh).
+template <int D, int G>
+__device__ __forceinline__ const float* shared_o_at(const DecodeArgs& a, int seq, int kvh, int h,
+                                                    int u, int d) {
+  return a.shared_o +
+         ((static_cast<int64_t>(kvh) * a.shared_units + u) * a.shared_rows_pad +
+          static_cast<int64_t>(seq) * G + h) * D + d;
+}
+
 // Placed at a 1024-byte-aligned address (the 128-byte swizzle repeats every
 // 1024 bytes and the panels must start on that boundary).
 template <int D, int G>
@@ -167,6 +221,9 @@ struct DecodeSmem {
   StageInfo job[3];
   alignas(8) uint64_t job_full[3];
   int abort_flag;
+  // Cascade decode: fold scratch of the merger and of the merge warp.
+  FoldScratch<G> fold_merger;
+  FoldScratch<G> fold_merge;
 };
 
 template <int D, int G>
@@ -174,11 +231,20 @@ constexpr size_t decode_smem_bytes() {
   return sizeof(DecodeSmem<D, G>) + 1024;  // slack for the 1024-byte alignment
 }
 
-// Chunks of each of sequence s's pairs: ceil(C / 32), and 1 for an empty
-// or out-of-range context (that chunk carries no tokens).
+// A context this kernel rejects: out of range, or (cascade decode) shorter
+// than the shared prefix.
+__device__ __forceinline__ bool bad_context(const DecodeArgs& a, int ctx, int max_ctx) {
+  return ctx < 0 || ctx > max_ctx || ctx < a.shared_len;
+}
+
+// Chunks of each of sequence s's pairs: ceil((C - shared_len) / 32) (the
+// tokens this kernel streams), and 1 for an empty private part or a rejected
+// context (that chunk carries no tokens).
 __device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int max_ctx) {
   const int ctx = a.context_lens[s];
-  return (ctx <= 0 || ctx > max_ctx) ? 1 : (ctx + kDecodeChunk - 1) / kDecodeChunk;
+  const int priv = ctx - a.shared_len;
+  return (bad_context(a, ctx, max_ctx) || priv <= 0) ? 1
+                                                      : (priv + kDecodeChunk - 1) / kDecodeChunk;
 }
 
 // The partial slot of the piece of a cut pair held by block cb2 (the pair
@@ -189,22 +255,45 @@ __device__ __forceinline__ int64_t piece_row(const StageInfo& inf, int cb2, int 
   return (static_cast<int64_t>(cb2) * 2 + sl) * G;
 }
 
+// Cascade decode, lane = dimension: scales a head's private accumulator
+// by fp and adds sum_u w_u o_u over the shared-prefix partial states (the
+// factors fold_head left in f).
+template <int D, int G>
+__device__ __forceinline__ void fold_acc(const DecodeArgs& a, int seq, int kvh, int h,
+                                         const FoldScratch<G>& f, float (&acc)[D / 32], int lane) {
+  const float fp = f.fp[h];
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) acc[i] *= fp;
+#pragma unroll 2
+  for (int u = 0; u < a.shared_units; ++u) {
+    const float w = f.w[h][u];
+    if (w == 0.f) continue;  // the same for every lane
+    const float* src = shared_o_at<D, G>(a, seq, kvh, h, u, lane);
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) acc[i] += w * __ldcg(src + i * 32);
+  }
+}
+
 // Merge of all pieces of a cut pair by one warp (log-sum-exp):
 //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
 // Pieces go to lanes in batches of 32, so every load of a pass is
 // independent of the others: lane j reads piece j's (m, l), the warp
 // reduces M and L, and the weights w_j = 2^(m_j - M) / L are broadcast by
-// shuffle while each lane accumulates its own dimensions.
+// shuffle while each lane accumulates its own dimensions.  In a cascade
+// decode the shared-prefix partial states are folded in the same way before
+// the division (f: this warp's fold scratch).
 template <int D, int G>
 __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long T, long long nb,
-                           int64_t row_base, int lane) {
+                           int64_t row_base, int lane, FoldScratch<G>& f) {
   const int n = inf.c_last - inf.c_first + 1;  // blocks spanned (empty ones hold no piece)
+  const bool cascade = a.shared_len > 0;
   if (n <= 32) {
     // Lane j holds piece j's (m, l) for every head: one round of loads.
     const int cb2 = inf.c_first + lane;
     const bool has = lane < n && slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
     const int64_t r = has ? piece_row(inf, cb2, G) : 0;
-    float w[G], inv[G];
+    float w[G], Mh[G], Lh[G];
+    bool badh[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float m = has ? __ldcg(a.part_ml + (r + h) * 2) : -INFINITY;
@@ -212,13 +301,14 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
       float M = m;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-      const float f = (has && M != -INFINITY) ? fast_exp2(m - M) : 0.f;
-      float L = l * f;
+      const float fw = (has && M != -INFINITY) ? fast_exp2(m - M) : 0.f;
+      float L = l * fw;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      const bool bad = __any_sync(0xffffffffu, l < 0.f);
-      inv[h] = (L > 0.f && !bad) ? 1.f / L : 0.f;
-      w[h] = f;
+      badh[h] = __any_sync(0xffffffffu, l < 0.f);
+      Mh[h] = M;
+      Lh[h] = L;
+      w[h] = fw;
     }
     // Lane = dimension: every piece's rows of every head, loads independent
     // of each other (an empty block's weight is 0 and its slot is selected
@@ -241,12 +331,26 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
         }
       }
     }
+    if (cascade) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+      for (int h = 0; h < G; ++h) fold_head<G>(a, inf.seq, inf.kvh, h, Mh[h], Lh[h], f, lane);
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        fold_acc<D, G>(a, inf.seq, inf.kvh, h, f, acc[h], lane);
+        Lh[h] = f.L[h];
+        badh[h] |= f.bad[h] != 0;
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float inv = (Lh[h] > 0.f && !badh[h]) ? 1.f / Lh[h] : 0.f;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i)
         static_cast<__nv_bfloat16*>(a.out)[(row_base + h) * D + i * 32 + lane] =
-            __float2bfloat16_rn(acc[h][i] * inv[h]);
+            __float2bfloat16_rn(acc[h][i] * inv);
+    }
     return;
   }
   for (int h = 0; h < G; ++h) {
@@ -273,7 +377,6 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
     // pass 2: out[d] = sum_j w_j o_j[d], weights broadcast by shuffle
     float acc[D / 32];
 #pragma unroll
@@ -296,6 +399,15 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
         }
       }
     }
+    if (cascade) {
+      fold_head<G>(a, inf.seq, inf.kvh, h, M, L, f, lane);
+      __syncwarp();
+      fold_acc<D, G>(a, inf.seq, inf.kvh, h, f, acc, lane);
+      L = f.L[h];
+      bad |= f.bad[h] != 0;
+      __syncwarp();
+    }
+    const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
 #pragma unroll
     for (int i = 0; i < D / 32; ++i)
       static_cast<__nv_bfloat16*>(a.out)[(row_base + h) * D + i * 32 + lane] =
@@ -458,11 +570,21 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int k = k0; k < k0 + n; ++k, ++c) {
           const int st = c % kStages;
           if (!claim(st)) return false;
-          const int tok = k * kDecodeChunk;
-          const int n_valid = (pbad_ctx || pctx <= 0) ? 0 : min(kDecodeChunk, pctx - tok);
+          const int tok = a.shared_len + k * kDecodeChunk;
+          const int n_valid = (pbad_ctx || pctx - tok <= 0) ? 0 : min(kDecodeChunk, pctx - tok);
           int id = 0;
           bool bad = pbad_ctx;
-          if (n_valid > 0) {
+          if (k == 0 && a.shared_len > 0 && !bad) {
+            // Cascade decode: the sequence's leading blocks must be the
+            // shared ones (table row 0's), whose partials are folded in.
+            for (int i = 0; i < a.shared_len / kBlockSize; ++i)
+              if (table[i] != a.block_tables[i]) {
+                bad = true;
+                report_error(a.err, kErrDeviceCheck, kSiteDecodeShared);
+                break;
+              }
+          }
+          if (n_valid > 0 && !bad) {
             id = table[tok >> 8];
             if (id < 0 || id >= a.num_blocks) {
               bad = true;
@@ -515,14 +637,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int enc = seq_chunks(a, eseq, max_ctx);
           const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
           if (epair_begin + enc > cb && epair_begin > ca) {
-            if (!emit_piece(eseq, ebase, ectx, ectx < 0 || ectx > max_ctx, enc, epair_begin, cb, 1))
+            if (!emit_piece(eseq, ebase, ectx, bad_context(a, ectx, max_ctx), enc, epair_begin, cb, 1))
               aborted = true;
             stop = epair_begin;
           }
         }
         long long base = sm.start_base * hkv;  // first chunk of seq's pairs
         int ctx = a.context_lens[seq];
-        bool ctx_bad = ctx < 0 || ctx > max_ctx;
+        bool ctx_bad = bad_context(a, ctx, max_ctx);
         int nch = seq_chunks(a, seq, max_ctx);
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
@@ -541,7 +663,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             ++seq;
             base = pair_end;
             ctx = a.context_lens[seq];
-            ctx_bad = ctx < 0 || ctx > max_ctx;
+            ctx_bad = bad_context(a, ctx, max_ctx);
             nch = seq_chunks(a, seq, max_ctx);
             if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
           }
@@ -863,16 +985,53 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       // The mailbox has been read: let the consumers post again.
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.mail_free));
+      // Cascade decode: a whole pair's private state is merged here with the
+      // shared-prefix partial states (log-sum-exp), before the division.
+      const bool fold = single && a.shared_len > 0 && !bad;
+      FoldScratch<G>& fs = sm.fold_merger;
+      if (fold) {
+#pragma unroll 1
+        for (int h = 0; h < G; ++h)
+          fold_head<G>(a, inf.seq, inf.kvh, h, __shfl_sync(0xffffffffu, hM, h),
+                       __shfl_sync(0xffffffffu, hL, h), fs, lane);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int v = lane + 32 * i;
+          if (v >= kVec) continue;
+          const int hh = (v * 4) / D;
+          const int d = v * 4 - hh * D;
+          const float fp = fs.fp[hh];
+          float4 acc = make_float4(res[i].x * fp, res[i].y * fp, res[i].z * fp, res[i].w * fp);
+#pragma unroll 4
+          for (int u = 0; u < a.shared_units; ++u) {
+            const float w = fs.w[hh][u];
+            if (w == 0.f) continue;
+            const float4 x =
+                __ldcg(reinterpret_cast<const float4*>(shared_o_at<D, G>(a, inf.seq, inf.kvh, hh, u, d)));
+            acc.x += w * x.x;
+            acc.y += w * x.y;
+            acc.z += w * x.z;
+            acc.w += w * x.w;
+          }
+          res[i] = acc;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
         const int v = lane + 32 * i;
         const int hh = (v * 4) / D;
-        const float L = __shfl_sync(0xffffffffu, hL, hh & 31);
+        float L = __shfl_sync(0xffffffffu, hL, hh & 31);
         const float M = __shfl_sync(0xffffffffu, hM, hh & 31);
         if (v >= kVec) continue;
         const int d = v * 4 - hh * D;
+        bool bad_row = bad;
+        if (fold) {
+          L = fs.L[hh];
+          bad_row = fs.bad[hh] != 0;
+        }
         if (single) {
-          const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+          const float inv = (L > 0.f && !bad_row) ? 1.f / L : 0.f;
           uint2 packed;
           packed.x = pack_bf16x2(res[i].x * inv, res[i].y * inv);
           packed.y = pack_bf16x2(res[i].z * inv, res[i].w * inv);
@@ -924,7 +1083,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       if (inf.flags & kEnd) break;
       fence_acq_rel_gpu();  // every lane: the other pieces' partials are visible
       const int64_t row_base = static_cast<int64_t>(inf.seq) * a.num_q_heads + inf.kvh * G;
-      merge_pair<D, G>(a, inf, T, nb, row_base, lane);
+      merge_pair<D, G>(a, inf, T, nb, row_base, lane, sm.fold_merge);
     }
   }
 }

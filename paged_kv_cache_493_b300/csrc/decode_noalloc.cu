@@ -6,10 +6,9 @@
 //  - Serving engines that give (nearly) all free device memory to the KV
 //    block pool at start-up: a workspace allocated later by the library can
 //    fail for lack of memory, or sit outside the engine's own accounting.
-//  - Code that runs while a stream is captured into a CUDA graph, where a
-//    cudaMalloc is not allowed.
 //  - Processes whose device memory must all go through one caching
-//    allocator.
+//    allocator, so that a library's private cudaMalloc would break its
+//    bookkeeping (or the allocator has already reserved the memory).
 // pkv_decode_attention grows a cudaMalloc'ed workspace on first need; this
 // entry point uses the static array below instead, and the caller still
 // passes every input and output.
@@ -28,16 +27,16 @@
 
 namespace {
 
-// Layout of the per-device scratch: a 256-byte word for the kernels'
-// device-side error reports; the decode kernel's counters in a fixed region
-// of their own (zero at load, never reset, never overlapped by other data
-// whatever the batch shape): a 256-byte header with the launch epoch, then 8
-// bytes per (sequence, KV head) pair; then two partial slots per decode
-// block of G * (head_dim + 2) fp32 values.
+// Layout of the per-device scratch: the decode kernel's counters in a fixed
+// region of their own (zero at load, never reset, never overlapped by other
+// data whatever the batch shape): a 256-byte header with the launch epoch,
+// then 8 bytes per (sequence, KV head) pair; then two partial slots per
+// decode block of G * (head_dim + 2) fp32 values.  Device-side check
+// failures and wait timeouts go to the library's error word (also a static
+// device variable), which pkv_get_device_error reads and clears.
 constexpr size_t kScratchBytes = size_t{16} << 20;
-constexpr size_t kErrBytes = 256;
 constexpr size_t kCounterBytes = (size_t{2} << 20) + 256;  // 262144 (sequence, KV head) pairs
-constexpr size_t kPartialBytes = kScratchBytes - kErrBytes - kCounterBytes;
+constexpr size_t kPartialBytes = kScratchBytes - kCounterBytes;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
@@ -48,14 +47,17 @@ struct NoAllocDevice {
   bool usable = false;
   int num_sms = 0;
   unsigned char* scratch = nullptr;  // device address of g_decode_scratch
+  pkv::DeviceError* err = nullptr;   // device address of the library's error word
 };
 
 std::mutex g_mu;
 NoAllocDevice g_dev[kMaxDevices];
 
 // Once per device, with that device current: check the architecture, find
-// the tensor-map encoder and look up the device address of the scratch.
-// Must be called with g_mu held.
+// the tensor-map encoder and look up the device addresses of the scratch and
+// of the error word.  A device that is not sm_103a is marked unusable for
+// good; a failed lookup is retried by the next call, so one refused first
+// call does not disable the entry point.  Must be called with g_mu held.
 NoAllocDevice* device_setup(pkv_status* st) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -65,18 +67,29 @@ NoAllocDevice* device_setup(pkv_status* st) {
   }
   NoAllocDevice& d = g_dev[dev];
   if (!d.ready) {
-    d.ready = true;
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    int major = 0, minor = 0, sms = 0;
+    const bool attrs =
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
     void* ptr = nullptr;
-    d.usable = major == 10 && minor == 3 && pkv::load_tensor_map_encoder() &&
-               cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess && ptr != nullptr;
-    d.scratch = static_cast<unsigned char*>(ptr);
+    if (attrs && !(major == 10 && minor == 3)) {
+      d.ready = true;  // not an sm_103a device: never usable
+      d.usable = false;
+    } else if (attrs && pkv::load_tensor_map_encoder() &&
+               cudaGetSymbolAddress(&ptr, g_decode_scratch) == cudaSuccess && ptr != nullptr) {
+      pkv::DeviceError* err = pkv::device_error_word();
+      if (err != nullptr) {
+        d.scratch = static_cast<unsigned char*>(ptr);
+        d.err = err;
+        d.num_sms = sms;
+        d.ready = true;
+        d.usable = true;
+      }
+    }
     cudaGetLastError();
   }
-  if (!d.usable) {
+  if (!d.ready || !d.usable) {
     *st = PKV_ERR_CUDA;
     return nullptr;
   }
@@ -97,12 +110,14 @@ extern "C" pkv_status pkv_decode_attention_noalloc(
   if (st != PKV_OK) return st;
   int num_sms = 0;
   unsigned char* scratch = nullptr;
+  pkv::DeviceError* err = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     NoAllocDevice* d = device_setup(&st);
     if (!d) return st;
     num_sms = d->num_sms;
     scratch = d->scratch;
+    err = d->err;
   }
   if (num_seqs == 0) return PKV_OK;
 
@@ -120,15 +135,15 @@ extern "C" pkv_status pkv_decode_attention_noalloc(
   a.scale = scale;
   a.out = out;
   a.wait_limit_ns = pkv::wait_limit_ns();
-  a.err = reinterpret_cast<pkv::DeviceError*>(scratch);
+  a.err = err;
   const int g = num_q_heads / num_kv_heads;
   const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
   a.num_ctas = pkv::decode_num_ctas(head_dim, g, num_sms, pairs, pkv::max_splits_setting());
   if (pkv::decode_counter_bytes(pairs) > kCounterBytes ||
       pkv::decode_partial_bytes(a.num_ctas, g, head_dim) > kPartialBytes)
     return PKV_ERR_UNSUPPORTED;
-  a.counters = reinterpret_cast<unsigned long long*>(scratch + kErrBytes);
-  a.part_o = reinterpret_cast<float*>(scratch + kErrBytes + kCounterBytes);
+  a.counters = reinterpret_cast<unsigned long long*>(scratch);
+  a.part_o = reinterpret_cast<float*>(scratch + kCounterBytes);
   a.part_ml = a.part_o + static_cast<size_t>(a.num_ctas) * 2 * g * head_dim;
 
   pkv::CacheMaps maps;

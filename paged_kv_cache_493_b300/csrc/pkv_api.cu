@@ -1,6 +1,12 @@
 // pkv_api.cu -- the extern "C" entry points of libpkv (declared in pkv.h):
 // host-side validation, per-device state (error word, decode workspace,
 // tensor-map cache), the split-K plan, and the kernel-timing profiler.
+//
+// The device error word is a file-scope __device__ variable: every device
+// that loads the library has its own copy, and no call has to allocate
+// memory to report a device-side check.  Host code reaches it through the
+// address cudaGetSymbolAddress gives for the current device (the variable's
+// name on the host is only a stand-in).
 #include <algorithm>
 #include <atomic>
 #include <cstdio>
@@ -20,6 +26,9 @@ using pkv::DeviceError;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMapCacheSize = 8;
+
+// One error word per device (first recorded error code and its site).
+__device__ DeviceError g_device_error;
 
 struct MapEntry {
   const void* k = nullptr;
@@ -104,7 +113,11 @@ bool load_encoder() {
   return true;
 }
 
-// Must be called with g_mu held.
+// Must be called with g_mu held.  Set-up allocates nothing: it checks the
+// architecture, finds the tensor-map encoder and looks up the device address
+// of the error word.  A device that is not sm_103a is marked unusable for
+// good; any other failure (a lookup refused while a stream is being
+// captured, say) is retried by the next call.
 DeviceState* device_state(pkv_status* st) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -114,21 +127,25 @@ DeviceState* device_state(pkv_status* st) {
   }
   DeviceState& d = g_dev[dev];
   if (!d.ready) {
-    d.ready = true;
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-    d.usable = (major == 10 && minor == 3) && load_encoder();
-    if (d.usable) {
-      if (cudaMalloc(&d.err, sizeof(DeviceError)) != cudaSuccess ||
-          cudaMemset(d.err, 0, sizeof(DeviceError)) != cudaSuccess) {
-        d.usable = false;
-      }
+    int major = 0, minor = 0, sms = 0;
+    const bool attrs =
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+    void* err = nullptr;
+    if (attrs && !(major == 10 && minor == 3)) {
+      d.ready = true;  // not an sm_103a device: never usable
+      d.usable = false;
+    } else if (attrs && load_encoder() &&
+               cudaGetSymbolAddress(&err, g_device_error) == cudaSuccess && err != nullptr) {
+      d.err = static_cast<DeviceError*>(err);
+      d.num_sms = sms;
+      d.ready = true;
+      d.usable = true;
     }
     cudaGetLastError();
   }
-  if (!d.usable) {
+  if (!d.ready || !d.usable) {
     *st = PKV_ERR_CUDA;
     return nullptr;
   }
@@ -232,6 +249,13 @@ bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t nu
 }
 
 bool load_tensor_map_encoder() { return load_encoder(); }
+
+DeviceError* device_error_word() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  pkv_status st;
+  DeviceState* ds = device_state(&st);
+  return ds ? ds->err : nullptr;
+}
 
 uint64_t wait_limit_ns() { return static_cast<uint64_t>(g_wait_limit_ns.load()); }
 

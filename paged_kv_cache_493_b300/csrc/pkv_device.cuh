@@ -26,6 +26,7 @@ enum ErrSite : int {
   kSiteDecodeWaitFull = 210,
   kSiteDecodeWaitEmpty = 211,
   kSiteDecodeWaitMerge = 212,
+  kSiteDecodeShared = 213,
   kSiteDecodeI8Context = 220,
   kSiteDecodeI8Block = 221,
   kSitePrefillChunk = 300,

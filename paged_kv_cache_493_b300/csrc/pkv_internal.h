@@ -57,7 +57,22 @@ struct DecodeArgs {
   float* part_ml;    // [num_ctas][2][G][2] (running max, sum)
   uint64_t wait_limit_ns;
   DeviceError* err;
+  // Cascade decode: the first shared_len tokens of every sequence (whole
+  // blocks, the same physical blocks as in table row 0) were attended by the
+  // shared-prefix kernel, which left shared_units partial states per row
+  // (layout of PrefillArgs::shared_o / shared_ml).  This kernel streams
+  // tokens [shared_len, context_lens[s]) only, checks that the sequence's
+  // leading table entries are row 0's, and folds the partials into each
+  // output.  shared_len = 0: plain decode.
+  int shared_len;
+  int shared_units;
+  int shared_rows_pad;
+  const float* shared_o;
+  const float* shared_ml;
 };
+
+// Most units (key ranges) the shared prefix of a cascade decode is cut into.
+constexpr int kMaxSharedUnits = 32;
 
 struct PrefillArgs {
   const void* q;
@@ -76,6 +91,18 @@ struct PrefillArgs {
   void* out;
   uint64_t wait_limit_ns;
   DeviceError* err;
+  // Shared-prefix role of the cascade decode (launch_shared_prefix only):
+  // the decode queries of all num_seqs sequences attend the first
+  // shared_tiles * 64 tokens reached through table row 0, cut into
+  // shared_units key ranges; row (s * G + g) of KV head h, unit u, leaves its
+  // partial state at index (h * shared_units + u) * shared_rows_pad + row of
+  // shared_o ([..][head_dim] fp32, unnormalised) and shared_ml ([..][2]: the
+  // reference max in the log2 domain and the sum; sum -1 marks a failed row).
+  int shared_tiles;
+  int shared_units;
+  int shared_rows_pad;  // row tiles * 128
+  float* shared_o;
+  float* shared_ml;
 };
 
 // INT8 KV cache: codes int8 [num_blocks][256][Hkv][D], scales float32
@@ -154,6 +181,10 @@ cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream);
+// The shared-prefix kernel of the cascade decode (qmap: the decode queries
+// viewed as {D, Hq, num_seqs} with the prefill's box).
+cudaError_t launch_shared_prefix(const PrefillArgs& a, const CacheMaps& maps,
+                                 const CUtensorMap& qmap, cudaStream_t stream);
 
 // Helpers shared by the C entry points (defined in pkv_api.cu).
 // Process-wide cap on the number of pieces a pair is cut into
@@ -167,6 +198,10 @@ pkv_status validate_attention_args(const void* q, int64_t q_row_stride, const vo
                                    int32_t d, const void* out);
 // Resolves cuTensorMapEncodeTiled from the driver (once); false if unavailable.
 bool load_tensor_map_encoder();
+// Device address of the current device's error word (a file-scope __device__
+// variable, looked up once per device; no allocation), or nullptr when the
+// device is unusable.  pkv_get_device_error reads and clears it.
+DeviceError* device_error_word();
 // Encodes the decode and prefill tensor maps of a cache (host only, no allocation).
 bool encode_cache_maps(CacheMaps* maps, const void* k, const void* v, int64_t num_blocks,
                        int num_kv_heads, int head_dim);

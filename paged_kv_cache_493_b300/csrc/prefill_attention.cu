@@ -120,7 +120,16 @@ __device__ __forceinline__ TileInfo find_tile(const PrefillArgs& a, int t, int q
   return ti;
 }
 
-template <int D, int G>
+// kShared = false: chunked causal prefill (grid: tiles x KV heads).
+// kShared = true: the shared-prefix role of the cascade decode (grid: row
+// tiles x units x KV heads).  The "queries" of a tile are then 128/G
+// sequences' decode queries (q viewed as [num_seqs][Hq][D]), the keys are
+// the unit's share of the shared prefix (the leading blocks of table row 0,
+// the same in every sharing sequence's table), nothing is masked, and the
+// epilogue writes each row's partial state -- the reference max m (log2
+// domain), the sum l and the unnormalised O, fp32 -- for the decode kernel
+// to merge with the sequence's private part.
+template <int D, int G, bool kShared>
 __global__ void __launch_bounds__(kPrefillThreads, kCtasPerSm)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, PrefillArgs a) {
@@ -146,7 +155,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kvh = blockIdx.x % a.num_kv_heads;
-  const int tile = blockIdx.x / a.num_kv_heads;
+  const int tile = kShared ? (blockIdx.x / a.num_kv_heads) / a.shared_units
+                           : blockIdx.x / a.num_kv_heads;
+  const int unit = kShared ? (blockIdx.x / a.num_kv_heads) % a.shared_units : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full, 1);
@@ -176,24 +187,42 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   grid_dependency_wait();
   grid_dependents_launch();
 
-  const TileInfo ti = find_tile(a, tile, QT);
+  TileInfo ti;
   const int max_ctx = a.max_blocks * kBlockSize;
   bool bad = false;
   int nkt = 0;
-  if (ti.valid) {
-    bad = ti.ctx < 0 || ti.ctx > max_ctx || ti.lq > ti.ctx || ti.q_row0 < 0 ||
-          static_cast<int64_t>(ti.q_row0) + ti.lq > a.total_q;
-    if (!bad) {
-      const int q_end = min(ti.qt_start + QT, ti.lq);      // one past the last real query
-      const int kmax = ti.ctx - ti.lq + q_end;              // keys the tile needs
-      nkt = (kmax + kKeyTile - 1) / kKeyTile;
+  int kbase = 0;  // first key of the CTA's range
+  if constexpr (kShared) {
+    // Tile `tile` holds sequences [tile * QT, tile * QT + QT); unit `unit`
+    // takes key tiles [t0, t1) of the shared prefix.
+    ti.seq = 0;
+    ti.qt_start = tile * QT;
+    ti.lq = a.num_seqs;
+    ti.ctx = a.shared_tiles * kKeyTile;
+    ti.q_row0 = 0;
+    ti.valid = ti.qt_start < a.num_seqs;
+    const int t0 = static_cast<int>(static_cast<int64_t>(unit) * a.shared_tiles / a.shared_units);
+    const int t1 =
+        static_cast<int>(static_cast<int64_t>(unit + 1) * a.shared_tiles / a.shared_units);
+    nkt = ti.valid ? t1 - t0 : 0;
+    kbase = t0 * kKeyTile;
+  } else {
+    ti = find_tile(a, tile, QT);
+    if (ti.valid) {
+      bad = ti.ctx < 0 || ti.ctx > max_ctx || ti.lq > ti.ctx || ti.q_row0 < 0 ||
+            static_cast<int64_t>(ti.q_row0) + ti.lq > a.total_q;
+      if (!bad) {
+        const int q_end = min(ti.qt_start + QT, ti.lq);      // one past the last real query
+        const int kmax = ti.ctx - ti.lq + q_end;              // keys the tile needs
+        nkt = (kmax + kKeyTile - 1) / kKeyTile;
+      }
     }
   }
   const int32_t* table = a.block_tables + static_cast<int64_t>(max(ti.seq, 0)) * a.max_blocks;
   if (warp == kProducerWarp && ti.valid && !bad) {
-    const int nblk = (nkt * kKeyTile + kBlockSize - 1) / kBlockSize;
+    const int nblk = (kbase + nkt * kKeyTile + kBlockSize - 1) / kBlockSize;
     bool b = false;
-    for (int i = lane; i < nblk; i += 32) {
+    for (int i = kbase / kBlockSize + lane; i < nblk; i += 32) {
       const int id = table[i];
       b |= (id < 0 || id >= a.num_blocks);
     }
@@ -218,7 +247,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                     ti.q_row0 + ti.qt_start);
       for (int j = 0; j < nkt; ++j) {
         const int st = j & 1;
-        const int k0 = j * kKeyTile;
+        const int k0 = kbase + j * kKeyTile;
         const int slot = table[k0 / kBlockSize] * kBlockSize + (k0 % kBlockSize);
         if (j >= kKvStages &&
             !mbar_wait(bar.k_empty[st], ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
@@ -247,7 +276,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       int v_last[2] = {-1, -1};
       for (int j = 0; j < nkt; ++j) {
         const int st = j & 1;
-        const int k0 = j * kKeyTile;
+        const int k0 = kbase + j * kKeyTile;
         const int slot = table[k0 / kBlockSize] * kBlockSize + (k0 % kBlockSize);
         if (j >= kKvStages &&
             !mbar_wait(bar.v_empty[st], ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
@@ -375,7 +404,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                            *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
       tmem_wait_ld();
       const int k0 = j * kKeyTile;  // key of x[0]
-      if ((k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx)) {
+      if (!kShared && ((k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx))) {
 #pragma unroll
         for (int c = 0; c < kKeyTile; ++c)
           if (k0 + c > lim) x[c] = masked;
@@ -467,7 +496,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
     }
     const bool epilogue = __shfl_sync(0xffffffffu, (ok && nkt > 0 && !misc[1]) ? 1 : 0, 0) != 0;
-    if (epilogue) {
+    if constexpr (kShared) {
+      // Partial state of row (sequence qi, head r % G) for the decode
+      // kernel's merge: unnormalised O, reference max m, sum l.  A row whose
+      // unit failed (rejected block id, expired wait) is marked l = -1.
+      const int64_t prow =
+          (static_cast<int64_t>(kvh) * a.shared_units + unit) * a.shared_rows_pad +
+          static_cast<int64_t>(tile) * kRows + r;
+      if (epilogue) {
+        tc_fence_after();
+        float* orow = a.shared_o + prow * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(trow + kOCol + c * 32, ov);
+          tmem_wait_ld();
+          if (row_real) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              *reinterpret_cast<uint4*>(orow + c * 32 + 4 * e) =
+                  make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
+          }
+        }
+        if (row_real) *reinterpret_cast<float2*>(a.shared_ml + prow * 2) = make_float2(m, l);
+      } else if (ti.valid && qi < ti.lq) {
+        *reinterpret_cast<float2*>(a.shared_ml + prow * 2) = make_float2(0.f, -1.f);
+      }
+    } else if (epilogue) {
       tc_fence_after();
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
@@ -507,11 +562,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool kShared>
 cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                      cudaStream_t stream) {
   using L = PrefillLayout<D>;
-  auto kern = prefill_kernel<D, G>;
+  auto kern = prefill_kernel<D, G, kShared>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
@@ -520,9 +575,16 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   constexpr int QT = kRows / G;
-  // Upper bound on the number of tiles: sum_s ceil(Lq_s / QT) <= total/QT + num_seqs.
-  const int64_t tiles = a.total_q / QT + a.num_seqs;
-  const int64_t blocks = tiles * a.num_kv_heads;
+  int64_t blocks;
+  if (kShared) {
+    // Row tiles of QT sequences x units x KV heads.
+    const int64_t tiles = (static_cast<int64_t>(a.num_seqs) + QT - 1) / QT;
+    blocks = tiles * a.shared_units * a.num_kv_heads;
+  } else {
+    // Upper bound on the number of tiles: sum_s ceil(Lq_s / QT) <= total/QT + num_seqs.
+    const int64_t tiles = a.total_q / QT + a.num_seqs;
+    blocks = tiles * a.num_kv_heads;
+  }
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -538,15 +600,15 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
   return cudaLaunchKernelEx(&cfg, kern, qmap, maps.k_sw128, maps.v_sw128, a);
 }
 
-template <int D>
+template <int D, bool kShared>
 cudaError_t launch_d(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                      cudaStream_t stream) {
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_t<D, 1>(a, maps, qmap, stream);
-    case 2: return launch_t<D, 2>(a, maps, qmap, stream);
-    case 4: return launch_t<D, 4>(a, maps, qmap, stream);
-    case 8: return launch_t<D, 8>(a, maps, qmap, stream);
-    case 16: return launch_t<D, 16>(a, maps, qmap, stream);
+    case 1: return launch_t<D, 1, kShared>(a, maps, qmap, stream);
+    case 2: return launch_t<D, 2, kShared>(a, maps, qmap, stream);
+    case 4: return launch_t<D, 4, kShared>(a, maps, qmap, stream);
+    case 8: return launch_t<D, 8, kShared>(a, maps, qmap, stream);
+    case 16: return launch_t<D, 16, kShared>(a, maps, qmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -556,8 +618,16 @@ cudaError_t launch_d(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  if (a.head_dim == 128) return launch_d<128>(a, maps, qmap, stream);
-  if (a.head_dim == 64) return launch_d<64>(a, maps, qmap, stream);
+  if (a.head_dim == 128) return launch_d<128, false>(a, maps, qmap, stream);
+  if (a.head_dim == 64) return launch_d<64, false>(a, maps, qmap, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_shared_prefix(const PrefillArgs& a, const CacheMaps& maps,
+                                 const CUtensorMap& qmap, cudaStream_t stream) {
+  if (a.shared_units <= 0 || a.shared_tiles <= 0) return cudaErrorInvalidValue;
+  if (a.head_dim == 128) return launch_d<128, true>(a, maps, qmap, stream);
+  if (a.head_dim == 64) return launch_d<64, true>(a, maps, qmap, stream);
   return cudaErrorInvalidValue;
 }
 

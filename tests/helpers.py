@@ -4,6 +4,7 @@ import numpy as np
 import torch
 
 import oracle
+import oracle.parallel as oracle_parallel
 import paged_kv_cache_493_b300 as pkv
 
 # bf16-in / fp32-accumulate attention against the fp64 oracle.
@@ -53,14 +54,22 @@ def run_prefill_step(case, stream=None):
 
 
 def oracle_decode_after_store(case, rows=None):
+    """The oracle's store, then its decode: the full output on every host core
+    (oracle.parallel, bit-identical to the single-threaded call), or the
+    listed (sequence, head) rows."""
     c = case.cache
     kc, vc = oracle.store_kvcache(case.k_new, case.v_new, case.slot_mapping, c.k_cache, c.v_cache)
+    if rows is None:
+        return oracle_parallel.decode(case.q, kc, vc, c.block_tables, c.context_lens, case.scale)
     return oracle.decode(case.q, kc, vc, c.block_tables, c.context_lens, case.scale, rows=rows)
 
 
 def oracle_prefill_after_store(case, rows=None):
     c = case.cache
     kc, vc = oracle.store_kvcache(case.k_new, case.v_new, case.slot_mapping, c.k_cache, c.v_cache)
+    if rows is None:
+        return oracle_parallel.prefill(case.q, kc, vc, c.block_tables, case.cu_seqlens_q,
+                                       c.context_lens, case.scale)
     return oracle.prefill(case.q, kc, vc, c.block_tables, case.cu_seqlens_q, c.context_lens,
                           case.scale, rows=rows)
 

@@ -56,3 +56,21 @@ def test_two_rank_replicas_on_gloo(tmp_path):
     assert {o["rank"] for o in outs} == {0, 1}
     assert all(o["world"] == 2 and o["max"] == 3.0 for o in outs)
     assert outs[0]["q0"] != outs[1]["q0"]          # each replica draws its own batch
+
+
+def test_reference_arm_under_two_ranks_prints_one_line():
+    """`bench.py --impl reference --gpus 2` starts two ranks itself (torchrun,
+    gloo here); rank 0 alone times the oracle and prints one JSON line, rank
+    1 exits 0 without work."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--steps", "1", "--warmup", "1"], env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = __import__("json").loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["cpu_baseline"]["cores"] >= 1 and line["value"] > 0

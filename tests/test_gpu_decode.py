@@ -43,16 +43,12 @@ def test_prefix_decode_b64_full(cuda_device):
     no_device_error()
 
 
-def test_long_decode_32k_sampled(cuda_device):
-    """Full size (16 x 32768, 2048-block pool, K x3); oracle on one head per sequence
-    plus every head of the first and last sequence."""
+def test_long_decode_32k_full(cuda_device):
+    """Full size (16 x 32768, 2048-block pool, K x3), every (sequence, head)
+    output against the oracle (run over the host cores)."""
     case = W.long_decode()
     out, _, _ = run_decode_step(case)
-    rows = [(s, (5 * s) % 16) for s in range(16)] + [(0, h) for h in range(16)] + \
-           [(15, h) for h in range(16)]
-    ref = oracle_decode_after_store(case, rows=rows)
-    got = torch.stack([out[s, h] for s, h in rows])
-    assert_close(got, ref, "long_decode_32k")
+    assert_close(out, oracle_decode_after_store(case), "long_decode_32k")
     no_device_error()
 
 

@@ -44,20 +44,12 @@ def test_prefill_ragged_batch_with_empty_chunks(cuda_device):
     no_device_error()
 
 
-def test_chunked_prefill_8x512_sampled(cuda_device):
-    """Full size (8 x 512 queries over 4608 keys, ~5% of slots -1); the oracle
-    computes the first and last query of every chunk for all heads, plus a
-    spread of rows across the chunks."""
+def test_chunked_prefill_8x512_full(cuda_device):
+    """Full size (8 x 512 queries over 4608 keys, ~5% of slots -1): every
+    (query, head) output against the oracle (run over the host cores)."""
     case = W.chunked_prefill()
     out, _, _ = run_prefill_step(case)
-    rows = []
-    for s in range(8):
-        for i in (0, 511):
-            rows += [(s * 512 + i, h) for h in range(16)]
-        rows += [(s * 512 + (37 * k + 11 * s) % 512, (3 * k + s) % 16) for k in range(12)]
-    ref = oracle_prefill_after_store(case, rows=rows)
-    got = torch.stack([out[t, h] for t, h in rows])
-    assert_close(got, ref, "chunked_prefill_8x512")
+    assert_close(out, oracle_prefill_after_store(case), "chunked_prefill_8x512")
     no_device_error()
 
 
