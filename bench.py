@@ -267,8 +267,9 @@ def time_steps(step, steps: int, flush: Flusher):
 
 # ----------------------------------------------------------------------------- GPU arm
 class DecodeBench:
-    def __init__(self, case, pkv):
+    def __init__(self, case, pkv, shared_blocks: int = 0):
         self.case, self.pkv = case, pkv
+        self.shared_blocks = int(shared_blocks)
         c = case.cache
         self.kc, self.vc = to_dev(c.k_cache), to_dev(c.v_cache)
         self.bt, self.cl = to_dev(c.block_tables), to_dev(c.context_lens)
@@ -281,7 +282,12 @@ class DecodeBench:
     def step(self):
         p = self.pkv
         p.pkv_store_kvcache(self.kn, self.vn, self.sm, self.kc, self.vc)
-        p.pkv_decode_attention(self.q, self.kc, self.vc, self.bt, self.cl, self.case.scale, self.out)
+        if self.shared_blocks > 0:
+            p.pkv_decode_attention_shared_prefix(self.q, self.kc, self.vc, self.bt, self.cl,
+                                                 self.case.scale, self.shared_blocks, self.out)
+        else:
+            p.pkv_decode_attention(self.q, self.kc, self.vc, self.bt, self.cl, self.case.scale,
+                                   self.out)
 
     def e2e_setup(self):
         """A step's inputs (q, new K/V rows, slot mapping, block tables,
@@ -494,22 +500,47 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
             continue
         case = make(seed=replica_seed(1003 if name.startswith("long") else 1004, rank))
         b = decode_step_bytes(case)
-        bench = DecodeBench(case, pkv)
+        shared = case.shared_prefix_blocks if name.startswith("prefix") else 0
+        bench = DecodeBench(case, pkv, shared_blocks=shared)
         for _ in range(3):
             bench.step()
-        kt = kernel_times(pkv, bench.step, steps, flush, ["decode"])
-        per, _ = time_steps(bench.step, steps, flush)
+        kt = kernel_times(pkv, bench.step, steps, flush, ["shared_prefix", "decode"])
+
+        def attn():
+            if shared:
+                pkv.pkv_decode_attention_shared_prefix(bench.q, bench.kc, bench.vc, bench.bt,
+                                                       bench.cl, case.scale, shared, bench.out)
+            else:
+                pkv.pkv_decode_attention(bench.q, bench.kc, bench.vc, bench.bt, bench.cl,
+                                         case.scale, bench.out)
+
+        # The step (store + attention) and the attention call alone, each
+        # captured as a CUDA graph and replayed (no host launch time inside).
+        per, _ = time_steps(capture_graph(bench.step), steps, flush)
+        aper, _ = time_steps(capture_graph(attn), steps, flush)
         ms = sum(per) / len(per)
-        dec_ms = sum(v[0] for v in kt.values()) / steps
+        dec_ms = sum(aper) / len(aper)
         entry = {"step_ms": round(ms, 5), "decode_ms": round(dec_ms, 5),
+                 "timing": "graph replays, L2 flushed before each",
+                 "kernel_ms_eager": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()
+                                     if v[1]},
                  "kv_bytes": b["kv"], "kv_gbs": round(b["kv"] / (dec_ms * 1e-3) / 1e9, 2),
                  "frac_of_hbm_peak": round(b["kv"] / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                  "tokens_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1)}
-        if name.startswith("prefix"):
+        if shared:
+            def plain():
+                pkv.pkv_decode_attention(bench.q, bench.kc, bench.vc, bench.bt, bench.cl,
+                                         case.scale, bench.out)
+
+            pper, _ = time_steps(capture_graph(plain), steps, flush)
             u = unique_kv_bytes(case)
-            entry["unique_kv_bytes"] = u
-            entry["unique_kv_gbs"] = round(u / (dec_ms * 1e-3) / 1e9, 2)
-            entry["unique_frac_of_hbm_peak"] = round(u / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)
+            entry.update({
+                "decode": f"pkv_decode_attention_shared_prefix ({shared} shared blocks): "
+                          "shared-prefix tcgen05 kernel + split-K decode of the private parts",
+                "unique_kv_bytes": u,
+                "unique_kv_gbs": round(u / (dec_ms * 1e-3) / 1e9, 2),
+                "unique_frac_of_hbm_peak": round(u / (dec_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "plain_decode_ms": round(sum(pper) / len(pper), 5)})
         res[name] = entry
         del bench
         torch.cuda.empty_cache()
@@ -532,20 +563,32 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
         pkv.pkv_store_kvcache(kn, vn, sm, kc, vc)
         pkv.pkv_prefill_attention(q, kc, vc, bt, cu, cl, case.scale, out)
 
+    def pcall():
+        pkv.pkv_prefill_attention(q, kc, vc, bt, cu, cl, case.scale, out)
+
+    def scall():
+        pkv.pkv_store_kvcache(kn, vn, sm, kc, vc)
+
     for _ in range(3):
         pstep()
     kt = kernel_times(pkv, pstep, steps, flush, ["store_kvcache", "prefill"])
-    per, _ = time_steps(pstep, steps, flush)
+    # Step, prefill call and store call each replayed from a CUDA graph.
+    per, _ = time_steps(capture_graph(pstep), steps, flush)
+    pper, _ = time_steps(capture_graph(pcall), steps, flush)
+    sper, _ = time_steps(capture_graph(scall), steps, flush)
     flops = prefill_flops(case)
-    pre_ms = kt["prefill"][0] / max(kt["prefill"][1], 1)
-    st_ms = kt["store_kvcache"][0] / max(kt["store_kvcache"][1], 1)
+    pre_ms = sum(pper) / len(pper)
+    st_ms = sum(sper) / len(sper)
     store_bytes = int((case.slot_mapping >= 0).sum()) * 8 * 128 * 2 * 2 * 2
     tf = flops / (pre_ms * 1e-3) / 1e12
     res["chunked_prefill_8x512"] = {
         "step_ms": round(sum(per) / len(per), 5), "prefill_ms": round(pre_ms, 5), "flops": flops,
+        "timing": "graph replays, L2 flushed before each",
         "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
         "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
-        "store_ms": round(st_ms, 5), "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
+        "kernel_ms_eager": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},
+        "store_ms": round(st_ms, 5), "store_bytes": store_bytes,
+        "store_gbs": round(store_bytes / (st_ms * 1e-3) / 1e9, 2)}
     return res
 
 
@@ -573,12 +616,17 @@ def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
         pkv.pkv_store_kvcache_int8(kn, vn, sm, kc, vc, ks, vs)
         pkv.pkv_decode_attention_int8(q, kc, vc, ks, vs, bt, cl, case.scale, out)
 
+    def dcall():
+        pkv.pkv_decode_attention_int8(q, kc, vc, ks, vs, bt, cl, case.scale, out)
+
     for _ in range(3):
         step()
+    pkv.pkv_reserve_workspace(case.num_seqs, int(case.q.shape[1]), d, int(c.block_tables.shape[1]))
     kt = kernel_times(pkv, step, steps, flush, ["store_kvcache_int8", "decode_int8"])
-    per, _ = time_steps(step, steps, flush)
+    per, _ = time_steps(capture_graph(step), steps, flush)
+    dper, _ = time_steps(capture_graph(dcall), steps, flush)
     ms = sum(per) / len(per)
-    dec_ms = kt["decode_int8"][0] / max(kt["decode_int8"][1], 1)
+    dec_ms = sum(dper) / len(dper)
     kv = int(c.context_lens.sum()) * hkv * (2 * d + 2 * 4)  # codes + one fp32 scale per row, K and V
     dec_bytes = kv + case.q.numel() * 2 * 2 + (c.block_tables.numel() + c.context_lens.numel()) * 4
     gbs = dec_bytes / (dec_ms * 1e-3) / 1e9

@@ -134,6 +134,53 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
                                 float scale, void* out, pkv_stream_t stream);
 
 /*
+ * pkv_decode_attention_shared_prefix -- pkv_decode_attention for a batch whose
+ * sequences share a prefix of whole blocks ("cascade" decode; ocdem.com
+ * nano-vllm article §2.1: sequences with a common prefix point at the same
+ * physical blocks, "高效的内存共享"; blog.hotdry.top "1200行代码挑战vLLM",
+ * §性能优化 1 前缀缓存).  Same arguments and result as pkv_decode_attention,
+ * plus
+ *
+ *   shared_blocks  the number of leading blocks every sequence shares: for
+ *                  every s, block_tables[s][i] == block_tables[0][i] for
+ *                  i < shared_blocks, and context_lens[s] >= 256 * shared_blocks
+ *                  (0 <= shared_blocks <= max_blocks_per_seq; 0 is exactly
+ *                  pkv_decode_attention).
+ *
+ * The shared blocks are read from HBM once for the whole batch instead of
+ * once per sequence: a tcgen05 kernel attends the queries of all sequences
+ * of a KV head (128 query rows per tile) to the shared keys, cut into key
+ * ranges ("units") that run in parallel on the CTAs of one thread-block
+ * cluster and are merged through distributed shared memory into one fp32
+ * partial state per query row (max, sum, unnormalised output); the split-K
+ * decode kernel then streams each sequence's private tokens
+ * [256 * shared_blocks, context_lens[s]) only and merges the shared partial
+ * state into the output by log-sum-exp.  The result equals
+ * pkv_decode_attention's up to fp32 rounding (softmax is invariant to how
+ * the keys are grouped).  A sequence whose leading table entries differ from
+ * row 0's, or whose context is shorter than the shared prefix, gets a zero
+ * output and PKV_ERR_DEVICE_CHECK.  Workspace as for pkv_decode_attention
+ * (plus the shared partial states, sized by pkv_reserve_workspace too).
+ * Two kernel launches on `stream`.
+ */
+pkv_status pkv_decode_attention_shared_prefix(const void* q, int64_t q_row_stride,
+                                              const void* k_cache, const void* v_cache,
+                                              int64_t num_blocks, const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t num_seqs,
+                                              int32_t num_q_heads, int32_t num_kv_heads,
+                                              int32_t head_dim, float scale,
+                                              int32_t shared_blocks, void* out,
+                                              pkv_stream_t stream);
+
+/* Key ranges (the CTAs of one cluster) the shared prefix of
+ * pkv_decode_attention_shared_prefix is cut into: 1, 2, 4, 8 or 16 (capped
+ * at the prefix's 64-key tiles), or 0 for automatic (the default: up to 8,
+ * about one CTA per SM).  Other values are PKV_ERR_INVALID_ARG.
+ * Process-wide. */
+pkv_status pkv_set_shared_prefix_units(int32_t units);
+
+/*
  * pkv_prefill_attention -- chunked causal prefill over cached blocks
  * (tuning guide §3.2: chunks bounded by max_num_batched_tokens; §2.2:
  * variable-length batches; intelliparadigm.com article §7.1 预填充阶段).

@@ -38,6 +38,9 @@ SIGNATURES = {
                                _I32, _F, _P, _P], _I32),
     "pkv_decode_attention_noalloc": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _I32, _I32, _I32,
                                       _I32, _F, _P, _P], _I32),
+    "pkv_decode_attention_shared_prefix": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
+                                            _I32, _I32, _F, _I32, _P, _P], _I32),
+    "pkv_set_shared_prefix_units": ([_I32], _I32),
     "pkv_store_kvcache_int8": ([_P, _P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32,
                                 _P], _I32),
     "pkv_decode_attention_int8": ([_P, _I64, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
@@ -168,6 +171,32 @@ def pkv_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale:
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
         _ptr(context_lens), b, hq, hkv, d, float(scale), _ptr(out), _stream(stream)),
         "pkv_decode_attention")
+
+
+def pkv_decode_attention_shared_prefix(q, k_cache, v_cache, block_tables, context_lens,
+                                       scale: float, shared_blocks: int, out,
+                                       stream=None) -> None:
+    """Cascade decode: as pkv_decode_attention for a batch whose sequences all
+    share their first ``shared_blocks`` table entries (and contexts at least
+    that long); the shared blocks are read once for the whole batch."""
+    nb, hkv, d = _cache(k_cache, v_cache)
+    _need(q.dim() == 3, "q: [B, Hq, D]")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    qs = _rows(q, "q", hq, d)
+    _i32(block_tables, "block_tables")
+    _i32(context_lens, "context_lens")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == b, "block_tables: [B, max_blocks]")
+    _need(context_lens.numel() == b, "context_lens: [B]")
+    _need(out.is_contiguous() and out.shape == q.shape and out.dtype == q.dtype and out.is_cuda,
+          "out: contiguous, same shape/dtype as q")
+    _check(load_library().pkv_decode_attention_shared_prefix(
+        _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
+        _ptr(context_lens), b, hq, hkv, d, float(scale), int(shared_blocks), _ptr(out),
+        _stream(stream)), "pkv_decode_attention_shared_prefix")
+
+
+def pkv_set_shared_prefix_units(n: int) -> None:
+    _check(load_library().pkv_set_shared_prefix_units(int(n)), "pkv_set_shared_prefix_units")
 
 
 def pkv_decode_attention_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

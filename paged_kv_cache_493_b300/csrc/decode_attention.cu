@@ -80,6 +80,7 @@ constexpr int kProducerWarp = 4;   // TMA issue
 constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
 constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum-exp over L2)
 constexpr int kDecodeThreads = 7 * 32;
+constexpr int kSliceTable = 1024;  // table entries of a slice's sequences kept in shared memory
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
@@ -221,6 +222,11 @@ struct DecodeSmem {
   StageInfo job[3];
   alignas(8) uint64_t job_full[3];
   int abort_flag;
+  // The launch generation is published by the merge warp (off the critical
+  // path) and read by the merger before its first count.
+  alignas(8) uint64_t gen_full;
+  // Table rows of the slice's sequences (when they fit).
+  int slice_tab[kSliceTable];
   // Cascade decode: fold scratch of the merger and of the merge warp.
   FoldScratch<G> fold_merger;
   FoldScratch<G> fold_merge;
@@ -255,6 +261,20 @@ __device__ __forceinline__ int64_t piece_row(const StageInfo& inf, int cb2, int 
   return (static_cast<int64_t>(cb2) * 2 + sl) * G;
 }
 
+// Cascade decode: whether sequence seq's leading table entries are row 0's
+// (the shared blocks whose partial states are folded into its output).
+// One warp, lanes compare entries in parallel; a sequence that does not
+// share them is reported and gets a zero output.
+__device__ __forceinline__ bool shares_prefix(const DecodeArgs& a, int seq, int lane) {
+  const int nsb = a.shared_len / kBlockSize;
+  const int32_t* t = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks;
+  bool same = true;
+  for (int i = lane; i < nsb; i += 32) same &= __ldg(t + i) == __ldg(a.block_tables + i);
+  const bool all = __all_sync(0xffffffffu, same);
+  if (!all && lane == 0) report_error(a.err, kErrDeviceCheck, kSiteDecodeShared);
+  return all;
+}
+
 // Cascade decode, lane = dimension: scales a head's private accumulator
 // by fp and adds sum_u w_u o_u over the shared-prefix partial states (the
 // factors fold_head left in f).
@@ -286,7 +306,8 @@ template <int D, int G>
 __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long T, long long nb,
                            int64_t row_base, int lane, FoldScratch<G>& f) {
   const int n = inf.c_last - inf.c_first + 1;  // blocks spanned (empty ones hold no piece)
-  const bool cascade = a.shared_len > 0;
+  const bool unshared = a.shared_len > 0 && !shares_prefix(a, inf.seq, lane);
+  const bool cascade = a.shared_len > 0 && !unshared;
   if (n <= 32) {
     // Lane j holds piece j's (m, l) for every head: one round of loads.
     const int cb2 = inf.c_first + lane;
@@ -305,7 +326,7 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
       float L = l * fw;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      badh[h] = __any_sync(0xffffffffu, l < 0.f);
+      badh[h] = __any_sync(0xffffffffu, l < 0.f) || unshared;
       Mh[h] = M;
       Lh[h] = L;
       w[h] = fw;
@@ -366,7 +387,7 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    bad = __any_sync(0xffffffffu, bad);
+    bad = __any_sync(0xffffffffu, bad) || unshared;
     float L = 0.f;
     for (int j0 = 0; j0 < n; j0 += 32) {
       const int cb2 = inf.c_first + j0 + lane;
@@ -447,6 +468,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     }
     mbar_init(smem_u32(&sm.mail_full), kConsumerWarps);
     mbar_init(smem_u32(&sm.mail_free), 1);
+    mbar_init(smem_u32(&sm.gen_full), 1);
     for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&sm.job_full[j]), 1);
     sm.abort_flag = 0;
     sm.start_seq = -1;
@@ -466,17 +488,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 
   const int max_ctx = a.max_blocks * kBlockSize;
   const int hkv = a.num_kv_heads;
-  // Launch generation: epoch + 1.  Each block reads the epoch, then counts
-  // itself on the start counter; the block that completes the count (so
-  // every block has read the epoch) advances the epoch for the next launch,
-  // which cannot start before this one ends.  Off the critical path: the
-  // atomics overlap the rest of the block's work.
-  if (threadIdx.x == 0) {
-    const unsigned long long gen = (__ldcg(a.counters) + 1) & kGenMask;
-    sm.gen = gen;
-    if (tagged_increment(a.counters + 1, gen) == gridDim.x)
-      atomicExch(a.counters, gen);  // epoch := generation
-  }
 
   // ---- prefix sums of the chunk counts over the sequences (whole block):
   // thread t owns sequences [seg0, seg1).
@@ -533,6 +544,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // The table rows of the slice's sequences, copied to shared memory by
+    // the whole warp at once when they fit, so the stream never waits on a
+    // table load.
+    const int tab_seq0 = sm.start_seq;
+    const bool tab_smem = tab_seq0 >= 0 && sm.end_seq >= tab_seq0 &&
+                          static_cast<int64_t>(sm.end_seq - tab_seq0 + 1) * a.max_blocks <=
+                              kSliceTable;
+    if (tab_smem) {
+      const int n = (sm.end_seq - tab_seq0 + 1) * a.max_blocks;
+      const int32_t* src = a.block_tables + static_cast<int64_t>(tab_seq0) * a.max_blocks;
+      for (int i = lane; i < n; i += 32) sm.slice_tab[i] = __ldg(src + i);
+    }
+    __syncwarp();
     if (lane == 0) {
       // Last post of each stage (copies or descriptor only): phases of one
       // barrier complete in order, so once that one is complete every copy
@@ -574,18 +598,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int n_valid = (pbad_ctx || pctx - tok <= 0) ? 0 : min(kDecodeChunk, pctx - tok);
           int id = 0;
           bool bad = pbad_ctx;
-          if (k == 0 && a.shared_len > 0 && !bad) {
-            // Cascade decode: the sequence's leading blocks must be the
-            // shared ones (table row 0's), whose partials are folded in.
-            for (int i = 0; i < a.shared_len / kBlockSize; ++i)
-              if (table[i] != a.block_tables[i]) {
-                bad = true;
-                report_error(a.err, kErrDeviceCheck, kSiteDecodeShared);
-                break;
-              }
-          }
           if (n_valid > 0 && !bad) {
-            id = table[tok >> 8];
+            id = tab_smem ? sm.slice_tab[(pseq - tab_seq0) * a.max_blocks + (tok >> 8)]
+                          : table[tok >> 8];
             if (id < 0 || id >= a.num_blocks) {
               bad = true;
               report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
@@ -930,6 +945,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // them:
     //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
     int n_jobs = 0;  // merges handed to the merge warp
+    bool gen_seen = false;  // lane 0: the launch generation has been published
     for (int k = 0;; ++k) {
       const bool got = mbar_wait_sleepy(smem_u32(&sm.mail_full), k & 1, a.wait_limit_ns, 200);
       if (!__all_sync(0xffffffffu, got)) {
@@ -987,7 +1003,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0) mbar_arrive(smem_u32(&sm.mail_free));
       // Cascade decode: a whole pair's private state is merged here with the
       // shared-prefix partial states (log-sum-exp), before the division.
-      const bool fold = single && a.shared_len > 0 && !bad;
+      const bool unshared = single && a.shared_len > 0 && !shares_prefix(a, inf.seq, lane);
+      const bool fold = single && a.shared_len > 0 && !bad && !unshared;
       FoldScratch<G>& fs = sm.fold_merger;
       if (fold) {
 #pragma unroll 1
@@ -1025,7 +1042,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const float M = __shfl_sync(0xffffffffu, hM, hh & 31);
         if (v >= kVec) continue;
         const int d = v * 4 - hh * D;
-        bool bad_row = bad;
+        bool bad_row = bad || unshared;
         if (fold) {
           L = fs.L[hh];
           bad_row = fs.bad[hh] != 0;
@@ -1054,7 +1071,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           pieces += slice_begin(cb2 + 1, T, nb) > slice_begin(cb2, T, nb);
         unsigned long long* cnt =
             a.counters + kPairCounterOffset + static_cast<int64_t>(inf.seq) * hkv + inf.kvh;
-        last = static_cast<int>(tagged_increment(cnt, sm.gen)) == pieces;
+        if (!gen_seen) {
+          // The merge warp publishes the launch generation at its start.
+          gen_seen = mbar_wait(smem_u32(&sm.gen_full), 0, kDrainLimitNs);
+          if (!gen_seen) report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
+        }
+        last = gen_seen && static_cast<int>(tagged_increment(cnt, sm.gen)) == pieces;
       }
       if (__shfl_sync(0xffffffffu, last, 0) && n_jobs < 2) {
         if (lane == 0) {
@@ -1073,6 +1095,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // Cut contexts whose last piece this block counted: merge all their
     // pieces from the partial slots.  Off the consumers' path: the partial
     // reads are L2 round trips, slow while the streams load the memory system.
+    if (lane == 0) {
+      // Launch generation: epoch + 1.  Each block reads the epoch, then
+      // counts itself on the start counter; the block that completes the
+      // count (so every block has read the epoch) advances the epoch for the
+      // next launch, which cannot start before this one ends.  Done here,
+      // off the stream's path; the merger waits for it before its first
+      // count.
+      const unsigned long long gen = (__ldcg(a.counters) + 1) & kGenMask;
+      sm.gen = gen;
+      mbar_arrive(smem_u32(&sm.gen_full));
+      if (tagged_increment(a.counters + 1, gen) == gridDim.x)
+        atomicExch(a.counters, gen);  // epoch := generation
+    }
     for (int j = 0; j < 3; ++j) {
       const bool got = mbar_wait_sleepy(smem_u32(&sm.job_full[j]), 0, a.wait_limit_ns, 500);
       if (!__all_sync(0xffffffffu, got)) {

@@ -48,6 +48,8 @@ struct DeviceState {
   size_t ws_bytes = 0;
   unsigned long long* cnt = nullptr;  // decode arrival counters (zeroed once)
   size_t cnt_bytes = 0;
+  float* sh = nullptr;  // cascade decode: shared-prefix partial states
+  size_t sh_bytes = 0;
   MapEntry maps[kMapCacheSize];
   uint64_t clock = 0;
 };
@@ -56,6 +58,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 pkv::EncodeTiledFn g_encode = nullptr;
 std::atomic<int> g_max_splits{0};
+std::atomic<int> g_shared_units{0};
 std::atomic<int64_t> g_wait_limit_ns{1000000000};
 
 // ------------------------------------------------------------------ profiler
@@ -224,6 +227,51 @@ pkv_status ensure_workspace(DeviceState* ds, size_t part_bytes, size_t cnt_bytes
     ds->cnt_bytes = cnt_bytes;
   }
   return PKV_OK;
+}
+
+// Grows the cascade decode's shared-prefix partial buffer.
+pkv_status ensure_shared_workspace(DeviceState* ds, size_t bytes) {
+  if (bytes <= ds->sh_bytes) return PKV_OK;
+  if (ds->sh) cudaFree(ds->sh);
+  ds->sh = nullptr;
+  ds->sh_bytes = 0;
+  if (cudaMalloc(&ds->sh, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_NO_MEMORY;
+  }
+  ds->sh_bytes = bytes;
+  return PKV_OK;
+}
+
+// Cascade decode plan: row tiles of 128 / G sequences, and the units (one
+// cluster of CTAs per row tile and KV head, a power of two up to 16) the
+// shared prefix's key tiles are cut into: a set value, or the most that
+// keep the grid within one CTA per SM (at most 8, the portable cluster
+// size).  The cluster merges its units, so one partial state per row
+// remains: bytes = KV heads x padded rows x (head_dim + 2) fp32.
+struct SharedPlan {
+  int tiles;     // row tiles
+  int units;
+  int rows_pad;  // tiles * 128
+  int key_tiles;
+  size_t bytes;
+};
+
+SharedPlan shared_plan(int num_seqs, int hkv, int group, int head_dim, int shared_blocks,
+                       int num_sms) {
+  SharedPlan p;
+  const int qt = 128 / group;
+  p.tiles = (num_seqs + qt - 1) / qt;
+  p.rows_pad = p.tiles * 128;
+  p.key_tiles = shared_blocks * (pkv::kBlockSize / pkv::kPrefillKeyTile);
+  const int set = g_shared_units.load();
+  const int want = set > 0 ? set : std::min(8, num_sms / std::max(1, hkv * p.tiles));
+  int u = 1;
+  while (u * 2 <= want && u * 2 <= p.key_tiles && u * 2 <= 16) u *= 2;
+  p.units = u;
+  const size_t rows = static_cast<size_t>(hkv) * p.rows_pad;
+  p.bytes = rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+  return p;
 }
 
 }  // namespace
@@ -462,6 +510,109 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
       timed_launch("decode", s, [&] { return pkv::launch_decode(a, m, s); }));
 }
 
+pkv_status pkv_decode_attention_shared_prefix(
+    const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+    int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, float scale, int32_t shared_blocks, void* out, pkv_stream_t stream) {
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_cache, v_cache, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  if (shared_blocks < 0 || shared_blocks > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
+  if (shared_blocks == 0)
+    return pkv_decode_attention(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                                max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, scale, out, stream);
+  pkv::DecodeArgs a{};
+  pkv::PrefillArgs sp{};
+  CacheMaps m;
+  CUtensorMap qmap;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0) return PKV_OK;
+    const CacheMaps* maps = cache_maps(ds, k_cache, v_cache, num_blocks, num_kv_heads, head_dim);
+    if (!maps) return PKV_ERR_CUDA;
+    m = *maps;
+    const int g = num_q_heads / num_kv_heads;
+    // The decode queries viewed as {D, Hq, num_seqs}: a box holds the G
+    // heads of one KV head for 128 / G sequences (128 MMA rows).
+    if (!encode_3d(&qmap, q, head_dim, num_q_heads, num_seqs,
+                   static_cast<uint64_t>(head_dim) * 2, static_cast<uint64_t>(q_row_stride) * 2,
+                   64, g, 128 / g, CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    const SharedPlan plan =
+        shared_plan(num_seqs, num_kv_heads, g, head_dim, shared_blocks, ds->num_sms);
+    st = ensure_shared_workspace(ds, plan.bytes);
+    if (st != PKV_OK) return st;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    const int num_ctas =
+        pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    st = ensure_workspace(ds, pkv::decode_partial_bytes(num_ctas, g, head_dim),
+                          pkv::decode_counter_bytes(pairs));
+    if (st != PKV_OK) return st;
+    float* sh_o = ds->sh;
+    float* sh_ml = sh_o + static_cast<size_t>(num_kv_heads) * plan.rows_pad * head_dim;
+    const uint64_t wait = static_cast<uint64_t>(g_wait_limit_ns.load());
+
+    sp.q = q;
+    sp.q_row_stride = q_row_stride;
+    sp.block_tables = block_tables;
+    sp.max_blocks = max_blocks_per_seq;
+    sp.num_seqs = num_seqs;
+    sp.total_q = num_seqs;
+    sp.num_q_heads = num_q_heads;
+    sp.num_kv_heads = num_kv_heads;
+    sp.head_dim = head_dim;
+    sp.num_blocks = num_blocks;
+    sp.scale = scale;
+    sp.wait_limit_ns = wait;
+    sp.err = ds->err;
+    sp.shared_tiles = plan.key_tiles;
+    sp.shared_units = plan.units;
+    sp.shared_rows_pad = plan.rows_pad;
+    sp.shared_o = sh_o;
+    sp.shared_ml = sh_ml;
+
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.wait_limit_ns = wait;
+    a.err = ds->err;
+    a.num_ctas = num_ctas;
+    a.counters = ds->cnt;
+    a.part_o = ds->ws;
+    a.part_ml = a.part_o + static_cast<size_t>(num_ctas) * 2 * g * head_dim;
+    a.shared_len = shared_blocks * pkv::kBlockSize;
+    a.shared_units = 1;  // the cluster merged the units: one state per row
+    a.shared_rows_pad = plan.rows_pad;
+    a.shared_o = sh_o;
+    a.shared_ml = sh_ml;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed_launch("shared_prefix", s,
+                               [&] { return pkv::launch_shared_prefix(sp, m, qmap, s); });
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(timed_launch("decode", s, [&] { return pkv::launch_decode(a, m, s); }));
+}
+
+pkv_status pkv_set_shared_prefix_units(int32_t units) {
+  if (units < 0 || units > 16 || (units & (units - 1))) return PKV_ERR_INVALID_ARG;
+  g_shared_units.store(units);
+  return PKV_OK;
+}
+
 pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void* k_cache,
                                  const void* v_cache, int64_t num_blocks,
                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -549,10 +700,14 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
   if (!ds) return st;
   // Worst case over the group sizes num_q_heads allows (the call does not
   // name num_kv_heads).
-  size_t part = 0, cnt = 0;
+  size_t part = 0, cnt = 0, shared = 0;
   for (int g = 1; g <= 16; g *= 2) {
     if (num_q_heads % g) continue;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * (num_q_heads / g);
+    // The cascade decode's shared-prefix partials, for a prefix of up to the
+    // whole table width.
+    shared = std::max(shared, shared_plan(std::max(num_seqs, 1), num_q_heads / g, g, head_dim,
+                                          max_blocks_per_seq, ds->num_sms).bytes);
     const int ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
     part = std::max(part, pkv::decode_partial_bytes(ctas, g, head_dim));
     // The INT8 decode keeps its split partials in the same workspace.
@@ -561,7 +716,9 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
                                                          g, head_dim));
     cnt = std::max(cnt, pkv::decode_counter_bytes(pairs));
   }
-  return ensure_workspace(ds, part, cnt);
+  const pkv_status st2 = ensure_workspace(ds, part, cnt);
+  if (st2 != PKV_OK) return st2;
+  return ensure_shared_workspace(ds, shared);
 }
 
 pkv_status pkv_set_wait_limit_ns(int64_t limit_ns) {

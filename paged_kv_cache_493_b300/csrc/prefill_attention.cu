@@ -65,7 +65,16 @@ struct PrefillLayout {
   // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
   //           p_full[2], pv_done[2], drain   (17 x 8 bytes) + misc words
   static constexpr int kMisc = kBar + 24 * 8;
-  static constexpr int kBytes = kMisc + 64;
+  // Shared-prefix role only: each row's (m, l) for the cluster merge, then
+  // the per-row merge factors of the rows this CTA merges.
+  static constexpr int kRowMl = kMisc + 64;              // float2 [128]
+  static constexpr int kMergeW = kRowMl + kRows * 8;     // float [128] (rows x units)
+  static constexpr int kMergeRow = kMergeW + kRows * 4;  // float M, L; int bad [<= 128]
+  static constexpr int kBytes = kMergeRow + kRows * 12;
+  // After the last PV the Q/K/V buffers are free: each row's O (fp32) is
+  // staged there for the cluster merge, rows padded by 4 floats.
+  static constexpr int kOStride = D + 4;
+  static_assert(kRows * kOStride * 4 <= kBar, "O staging fits in the Q/K/V buffers");
 };
 
 struct PrefillBars {
@@ -154,10 +163,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kvh = blockIdx.x % a.num_kv_heads;
-  const int tile = kShared ? (blockIdx.x / a.num_kv_heads) / a.shared_units
+  // Shared-prefix role: the shared_units CTAs of one (row tile, KV head) are
+  // consecutive, one cluster; unit = rank in the cluster.
+  const int kvh = kShared ? (blockIdx.x / a.shared_units) % a.num_kv_heads
+                          : blockIdx.x % a.num_kv_heads;
+  const int tile = kShared ? (blockIdx.x / a.shared_units) / a.num_kv_heads
                            : blockIdx.x / a.num_kv_heads;
-  const int unit = kShared ? (blockIdx.x / a.num_kv_heads) % a.shared_units : 0;
+  const int unit = kShared ? blockIdx.x % a.shared_units : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full, 1);
@@ -497,30 +509,27 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     const bool epilogue = __shfl_sync(0xffffffffu, (ok && nkt > 0 && !misc[1]) ? 1 : 0, 0) != 0;
     if constexpr (kShared) {
-      // Partial state of row (sequence qi, head r % G) for the decode
-      // kernel's merge: unnormalised O, reference max m, sum l.  A row whose
-      // unit failed (rejected block id, expired wait) is marked l = -1.
-      const int64_t prow =
-          (static_cast<int64_t>(kvh) * a.shared_units + unit) * a.shared_rows_pad +
-          static_cast<int64_t>(tile) * kRows + r;
+      // This unit's partial state of row r (sequence qi, head r % G) --
+      // unnormalised O, reference max m, sum l -- is staged in shared
+      // memory for the cluster merge below.  A row whose unit failed
+      // (rejected block id, expired wait) is marked l = -1.
+      float2* row_ml = reinterpret_cast<float2*>(sgen + L::kRowMl);
       if (epilogue) {
         tc_fence_after();
-        float* orow = a.shared_o + prow * D;
+        float* orow = reinterpret_cast<float*>(sgen) + r * L::kOStride;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld_32x32b_x32(trow + kOCol + c * 32, ov);
           tmem_wait_ld();
-          if (row_real) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              *reinterpret_cast<uint4*>(orow + c * 32 + 4 * e) =
-                  make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
-          }
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<uint4*>(orow + c * 32 + 4 * e) =
+                make_uint4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
         }
-        if (row_real) *reinterpret_cast<float2*>(a.shared_ml + prow * 2) = make_float2(m, l);
-      } else if (ti.valid && qi < ti.lq) {
-        *reinterpret_cast<float2*>(a.shared_ml + prow * 2) = make_float2(0.f, -1.f);
+        row_ml[r] = make_float2(m, l);
+      } else {
+        row_ml[r] = make_float2(0.f, -1.f);
       }
     } else if (epilogue) {
       tc_fence_after();
@@ -560,6 +569,81 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+
+  if constexpr (kShared) {
+    // ---- cluster merge of the units' partial states (log-sum-exp):
+    //   M = max_u m_u, L = sum_u l_u 2^(m_u - M), O = sum_u O_u 2^(m_u - M)
+    // CTA of rank c merges rows [c R, c R + R), R = 128 / units, reading the
+    // other units' staged rows from their shared memory, and writes the
+    // merged state of each real row to global memory (a row any unit failed
+    // on is marked l = -1).  Every thread of every CTA of the cluster passes
+    // both cluster barriers (no early exit above in this role).
+    const int U = a.shared_units;
+    const int R = kRows / U;
+    const uint32_t rank = cluster_ctarank();
+    const int row0 = static_cast<int>(rank) * R;
+    const uint32_t s_ml = sbase + L::kRowMl;
+    float* mw = reinterpret_cast<float*>(sgen + L::kMergeW);         // [R][U]
+    float* mrow = reinterpret_cast<float*>(sgen + L::kMergeRow);     // M [R], L [R]
+    int* mbad = reinterpret_cast<int*>(sgen + L::kMergeRow + 8 * R);  // [R]
+    cluster_sync_all();  // every unit's rows are staged
+    constexpr int kMaxUnits = 16;
+    if (static_cast<int>(threadIdx.x) < R) {
+      // All units' (m, l) of the row in one round of remote loads.
+      const int row = row0 + threadIdx.x;
+      float2 ml[kMaxUnits];
+#pragma unroll
+      for (int u = 0; u < kMaxUnits; ++u)
+        ml[u] = u < U ? dsmem_ld_f2(dsmem_map(s_ml + row * 8, u)) : make_float2(-INFINITY, 0.f);
+      float M = -INFINITY;
+      bool bad = false;
+#pragma unroll
+      for (int u = 0; u < kMaxUnits; ++u) {
+        M = fmaxf(M, ml[u].x);
+        bad |= ml[u].y < 0.f;
+      }
+      float Ls = 0.f;
+#pragma unroll
+      for (int u = 0; u < kMaxUnits; ++u) {
+        const float w = (M == -INFINITY || ml[u].x == -INFINITY) ? 0.f : fast_exp2(ml[u].x - M);
+        if (u < U) mw[threadIdx.x * U + u] = w;
+        Ls += ml[u].y * w;
+      }
+      mrow[threadIdx.x] = M;
+      mrow[R + threadIdx.x] = Ls;
+      mbad[threadIdx.x] = bad ? 1 : 0;
+    }
+    __syncthreads();
+    const int64_t prow0 = static_cast<int64_t>(kvh) * a.shared_rows_pad +
+                          static_cast<int64_t>(tile) * kRows + row0;
+    const int real_rows = min(R, max(0, a.num_seqs * G - (tile * kRows + row0)));
+    constexpr int kGroups = D / 4;
+    for (int i = threadIdx.x; i < real_rows * kGroups; i += kPrefillThreads) {
+      const int rr = i / kGroups, g4 = (i % kGroups) * 4;
+      const uint32_t src = sbase + static_cast<uint32_t>(((row0 + rr) * L::kOStride + g4) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!mbad[rr]) {
+        // Every unit's four values in one round of remote loads.
+        float4 x[kMaxUnits];
+#pragma unroll
+        for (int u = 0; u < kMaxUnits; ++u)
+          x[u] = u < U ? dsmem_ld_f4(dsmem_map(src, u)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kMaxUnits; ++u) {
+          const float w = u < U ? mw[rr * U + u] : 0.f;
+          acc.x += w * x[u].x;
+          acc.y += w * x[u].y;
+          acc.z += w * x[u].z;
+          acc.w += w * x[u].w;
+        }
+      }
+      *reinterpret_cast<float4*>(a.shared_o + (prow0 + rr) * D + g4) = acc;
+      if (g4 == 0)
+        *reinterpret_cast<float2*>(a.shared_ml + (prow0 + rr) * 2) =
+            make_float2(mrow[rr], mbad[rr] ? -1.f : mrow[R + rr]);
+    }
+    cluster_sync_all();  // no CTA leaves while others read its shared memory
+  }
 }
 
 template <int D, int G, bool kShared>
@@ -588,15 +672,28 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
+  if (kShared) {
+    // The units of one (row tile, KV head) form a cluster (merged through
+    // distributed shared memory); more than 8 needs the non-portable size.
+    if (a.shared_units > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.shared_units);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kPrefillThreads);
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, qmap, maps.k_sw128, maps.v_sw128, a);
 }
 
@@ -625,7 +722,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CU
 
 cudaError_t launch_shared_prefix(const PrefillArgs& a, const CacheMaps& maps,
                                  const CUtensorMap& qmap, cudaStream_t stream) {
-  if (a.shared_units <= 0 || a.shared_tiles <= 0) return cudaErrorInvalidValue;
+  if (a.shared_units <= 0 || a.shared_units > 16 || (a.shared_units & (a.shared_units - 1)) ||
+      a.shared_tiles < a.shared_units)
+    return cudaErrorInvalidValue;
   if (a.head_dim == 128) return launch_d<128, true>(a, maps, qmap, stream);
   if (a.head_dim == 64) return launch_d<64, true>(a, maps, qmap, stream);
   return cudaErrorInvalidValue;

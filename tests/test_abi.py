@@ -55,6 +55,11 @@ def test_knobs_validate_arguments(lib):
     assert lib.pkv_profiler_enable(0) == pkv.PKV_OK
     assert lib.pkv_profiler_reset() == pkv.PKV_OK
     assert lib.pkv_reserve_workspace(4, 4, 96, 2) == pkv.PKV_ERR_INVALID_ARG
+    for bad in (-1, 3, 5, 32):
+        assert lib.pkv_set_shared_prefix_units(bad) == pkv.PKV_ERR_INVALID_ARG
+    for good in (0, 1, 2, 4, 8, 16):
+        assert lib.pkv_set_shared_prefix_units(good) == pkv.PKV_OK
+    assert lib.pkv_set_shared_prefix_units(0) == pkv.PKV_OK
     ms, n = ctypes.c_double(), ctypes.c_int64()
     assert lib.pkv_profiler_read(b"decode", ctypes.byref(ms), ctypes.byref(n)) == pkv.PKV_OK
     assert n.value == 0
