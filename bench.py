@@ -4,11 +4,13 @@
 
 One step = one pass of the hot path over the 128-sequence Qwen3-0.6B-like
 decode batch (16 q / 8 KV heads, head_dim 128, contexts U[100, 1024], 256-token
-blocks in a 1024-block pool): pkv_store_kvcache of the new K/V row of every
-sequence, then pkv_decode_attention (one split-K kernel; contexts cut across
-blocks are merged in-kernel by log-sum-exp).  The timed step is the pair of
-calls captured once as a CUDA graph and replayed, as a serving engine replays
-its decode step; the eager (uncaptured) time is reported beside it.
+blocks in a 1024-block pool): the store of the new K/V row of every sequence
+and the decode attention over the cache, done by pkv_decode_attention_append in
+one split-K kernel (contexts cut across blocks are merged in-kernel by
+log-sum-exp).  The timed step is that call captured once as a CUDA graph and
+replayed, as a serving engine replays its decode step; the eager (uncaptured)
+time and the same step as two calls (pkv_store_kvcache, then
+pkv_decode_attention) are reported beside it.
 The metric is KV GB/s (algorithmic bytes / step time) with decode tokens/s per
 layer beside it.  The long-context decode, prefix-sharing decode and chunked
 prefill workloads are measured too and reported under "other_workloads", with
@@ -56,11 +58,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # of the capture: the figure is reported only while the sources still hash to
 # that value (any change to the kernel makes it null until captured again).
 KERNEL_SOURCES = {
-    "decode_split": ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h"),
+    "decode_append": ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h"),
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_split": (None, MAIN_WORKLOAD, None),
+    "decode_append": (None, MAIN_WORKLOAD, None),
 }
 
 
@@ -279,6 +281,11 @@ class DecodeBench:
         pkv.pkv_reserve_workspace(case.num_seqs, int(case.q.shape[1]), int(case.q.shape[2]),
                                   int(c.block_tables.shape[1]))
 
+    def fused_step(self):
+        """The decode step as one kernel: store of the new rows and attention."""
+        self.pkv.pkv_decode_attention_append(self.q, self.kn, self.vn, self.sm, self.kc, self.vc,
+                                             self.bt, self.cl, self.case.scale, self.out)
+
     def step(self):
         p = self.pkv
         p.pkv_store_kvcache(self.kn, self.vn, self.sm, self.kc, self.vc)
@@ -318,8 +325,8 @@ class DecodeBench:
         p = self.pkv
         self.d_buf.copy_(self.h_buf, non_blocking=True)
         q, kn, vn, sm, bt, cl = self.d_in
-        p.pkv_store_kvcache(kn, vn, sm, self.kc, self.vc)
-        p.pkv_decode_attention(q, self.kc, self.vc, bt, cl, self.case.scale, self.out)
+        p.pkv_decode_attention_append(q, kn, vn, sm, self.kc, self.vc, bt, cl, self.case.scale,
+                                      self.out)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def e2e_phases(self, steps: int, flush) -> dict:
@@ -335,8 +342,8 @@ class DecodeBench:
             self.d_buf.copy_(self.h_buf, non_blocking=True)
             ev[1].record(stream)
             q, kn, vn, sm, bt, cl = self.d_in
-            p.pkv_store_kvcache(kn, vn, sm, self.kc, self.vc)
-            p.pkv_decode_attention(q, self.kc, self.vc, bt, cl, self.case.scale, self.out)
+            p.pkv_decode_attention_append(q, kn, vn, sm, self.kc, self.vc, bt, cl,
+                                          self.case.scale, self.out)
             ev[2].record(stream)
             self.h_out.copy_(self.out, non_blocking=True)
             ev[3].record(stream)
@@ -392,19 +399,28 @@ def run_gpu(args, rank, world, local):
         bench.step()
     torch.cuda.synchronize()
 
-    replay = capture_graph(bench.step)
+    # The step: pkv_decode_attention_append (store of the new rows and the
+    # split-K decode in one kernel), captured once as a graph and replayed;
+    # the two-call step (pkv_store_kvcache + pkv_decode_attention) beside it.
+    for _ in range(args.warmup):
+        bench.fused_step()
+    replay = capture_graph(bench.fused_step)
+    replay2 = capture_graph(bench.step)
     for _ in range(args.warmup):
         replay()
+        replay2()
     with ClockSampler(local) as clk:
         per, wall = time_steps(replay, args.steps, flush)
-        eager_per, _ = time_steps(bench.step, args.steps, flush)
-        names = ["store_kvcache", "decode"]
-        kt = kernel_times(pkv, bench.step, args.steps, flush, names)
+        eager_per, _ = time_steps(bench.fused_step, args.steps, flush)
+        kt = kernel_times(pkv, bench.fused_step, args.steps, flush, ["decode_append"])
+        two_per, _ = time_steps(replay2, args.steps, flush)
+        kt2 = kernel_times(pkv, bench.step, args.steps, flush, ["store_kvcache", "decode"])
     step_ms = reduce_max(sum(per) / len(per))
     eager_ms = reduce_max(sum(eager_per) / len(eager_per))
+    two_ms = reduce_max(sum(two_per) / len(two_per))
     value = world * bytes_["step"] / (step_ms * 1e-3) / 1e9
-    split_ms = kt["decode"][0] / max(kt["decode"][1], 1)
-    achieved = bytes_["split_kernel"] / (split_ms * 1e-3) / 1e9
+    split_ms = kt["decode_append"][0] / max(kt["decode_append"][1], 1)
+    achieved = bytes_["step"] / (split_ms * 1e-3) / 1e9
     launches_per_step = sum(n for _, n in kt.values()) / args.steps
 
     # End to end through the C ABI from pinned host buffers: one packed
@@ -447,7 +463,7 @@ def run_gpu(args, rank, world, local):
             "workload": MAIN_WORKLOAD, "num_seqs": case.num_seqs, "context_lens": "U[100,1024] seeded",
             "mean_context": round(float(case.cache.context_lens.float().mean()), 1),
             "num_q_heads": 16, "num_kv_heads": 8, "head_dim": 128, "block_size": 256,
-            "num_blocks": case.cache.num_blocks, "step": "store_kvcache + decode (one split-K kernel with in-kernel merge), replayed as a CUDA graph",
+            "num_blocks": case.cache.num_blocks, "step": "pkv_decode_attention_append: store of the new K/V rows + split-K decode with in-kernel merge, one kernel, replayed as a CUDA graph",
             "l2": "flushed before every step (256 MiB write, then a 256 MiB read of another buffer that drains the written lines), step timed alone",
             "parallelism": f"replicas{world}",
         },
@@ -457,18 +473,21 @@ def run_gpu(args, rank, world, local):
         "frac_of_nominal_8tbs": round(value / world / 8000.0, 4),
         "wall_s_timed_region": round(wall, 4),
         "eager_ms_per_step": round(eager_ms, 5),
+        "two_call_step": {"calls": "pkv_store_kvcache + pkv_decode_attention (graph)",
+                          "ms_per_step": round(two_ms, 5),
+                          "kernel_ms": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt2.items()}},
         "roofline": {
-            "kernel": "decode_split",
+            "kernel": "decode_split (fused store: pkv_decode_attention_append)",
             "bound": "hbm",
             "achieved": round(achieved, 2),
             "peak": peaks["hbm_gbs"],
             "peak_source": f"{peak_src} hbm_gbs (burst copy)",
             "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": captured_traffic("decode_split", MAIN_WORKLOAD),
+            "traffic": captured_traffic("decode_append", MAIN_WORKLOAD),
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, "
                               "valid only for the kernel sources it was captured on",
-            "algorithmic_bytes_per_launch": bytes_["split_kernel"],
+            "algorithmic_bytes_per_launch": bytes_["step"],
             "avg_launch_ms": round(split_ms, 5),
             "kernel_ms": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},
         },

@@ -134,6 +134,41 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
                                 float scale, void* out, pkv_stream_t stream);
 
 /*
+ * pkv_decode_attention_append -- one decode step's store and attention in one
+ * kernel: the same result as pkv_store_kvcache(k_new, v_new, k_row_stride,
+ * v_row_stride, slot_mapping, num_seqs, ...) followed by pkv_decode_attention
+ * (tuning guide §2.2: store_kvcache writes the new rows, attention then reads
+ * the cache; intelliparadigm.com article §7.1: each decode step appends one
+ * token's K/V to the cache).
+ *
+ *   k_new, v_new  bf16 [num_seqs][*]: row s (at k_new + s * k_row_stride) is
+ *                 sequence s's new token, the one at position
+ *                 context_lens[s] - 1, num_kv_heads * head_dim values.
+ *   slot_mapping  int32 [num_seqs]: the cache slot of that position, or -1
+ *                 to store nothing for the sequence.  Any other value is
+ *                 not stored and is reported as PKV_ERR_DEVICE_CHECK (the
+ *                 attention then reads the pool row as it stands, as for -1).
+ *   k_cache, v_cache  updated in place at those slots (bit-exact copies).
+ *   other arguments as for pkv_decode_attention.
+ *
+ * The block that streams the chunk holding position context_lens[s] - 1 of
+ * (sequence s, KV head h) copies head h of the new row in with the chunk,
+ * writes it to the cache and uses it in place of the pool row it loaded, so
+ * the step is one launch and the new rows cross HBM once.  The new token's
+ * slot must not lie in another sequence's context (it is a private block's
+ * next slot in a decode step).
+ */
+pkv_status pkv_decode_attention_append(const void* q, int64_t q_row_stride, const void* k_new,
+                                       const void* v_new, int64_t k_row_stride,
+                                       int64_t v_row_stride, const int32_t* slot_mapping,
+                                       void* k_cache, void* v_cache, int64_t num_blocks,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, float scale, void* out,
+                                       pkv_stream_t stream);
+
+/*
  * pkv_decode_attention_shared_prefix -- pkv_decode_attention for a batch whose
  * sequences share a prefix of whole blocks ("cascade" decode; ocdem.com
  * nano-vllm article §2.1: sequences with a common prefix point at the same

@@ -41,6 +41,8 @@ SIGNATURES = {
     "pkv_decode_attention_shared_prefix": ([_P, _I64, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
                                             _I32, _I32, _F, _I32, _P, _P], _I32),
     "pkv_set_shared_prefix_units": ([_I32], _I32),
+    "pkv_decode_attention_append": ([_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _I64, _P, _I32, _P,
+                                     _I32, _I32, _I32, _I32, _F, _P, _P], _I32),
     "pkv_store_kvcache_int8": ([_P, _P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _I32, _I32,
                                 _P], _I32),
     "pkv_decode_attention_int8": ([_P, _I64, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
@@ -193,6 +195,32 @@ def pkv_decode_attention_shared_prefix(q, k_cache, v_cache, block_tables, contex
         _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]),
         _ptr(context_lens), b, hq, hkv, d, float(scale), int(shared_blocks), _ptr(out),
         _stream(stream)), "pkv_decode_attention_shared_prefix")
+
+
+def pkv_decode_attention_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                                context_lens, scale: float, out, stream=None) -> None:
+    """One decode step in one kernel: store row s of k_new / v_new [B, Hkv, D]
+    (sequence s's new token, at position context_lens[s] - 1) at
+    slot_mapping[s] (-1: not stored), then decode q [B, Hq, D] -> out."""
+    nb, hkv, d = _cache(k_cache, v_cache)
+    _need(q.dim() == 3, "q: [B, Hq, D]")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    qs = _rows(q, "q", hq, d)
+    ks = _rows(k_new, "k_new", hkv, d)
+    vs = _rows(v_new, "v_new", hkv, d)
+    _need(k_new.shape[0] == b and v_new.shape[0] == b, "k_new, v_new: one row per sequence")
+    for x, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (slot_mapping, "slot_mapping")):
+        _i32(x, n)
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == b, "block_tables: [B, max_blocks]")
+    _need(context_lens.numel() == b and slot_mapping.numel() == b,
+          "context_lens, slot_mapping: [B]")
+    _need(out.is_contiguous() and out.shape == q.shape and out.dtype == q.dtype and out.is_cuda,
+          "out: contiguous, same shape/dtype as q")
+    _check(load_library().pkv_decode_attention_append(
+        _ptr(q), qs, _ptr(k_new), _ptr(v_new), ks, vs, _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), nb, _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), b,
+        hq, hkv, d, float(scale), _ptr(out), _stream(stream)), "pkv_decode_attention_append")
 
 
 def pkv_set_shared_prefix_units(n: int) -> None:

@@ -81,6 +81,7 @@ constexpr int kMergerWarp = 5;     // combines the consumers' states, writes res
 constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum-exp over L2)
 constexpr int kDecodeThreads = 7 * 32;
 constexpr int kSliceTable = 1024;  // table entries of a slice's sequences kept in shared memory
+constexpr int kSliceSlots = 256;   // fused store: slots of a slice's sequences kept likewise
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
@@ -88,6 +89,9 @@ struct StageInfo {
   int seq, kvh, slot, n_valid, flags;
   int c_first, c_last;  // blocks holding the pair's first and last chunk
   int first_slot;       // partial slot of the pair's piece in block c_first
+  // Fused store: the cache slot of the sequence's new token when this chunk
+  // holds it and its row is to be stored (else -1), and its row in the chunk.
+  int store_slot, store_row;
 };
 constexpr int kFirst = 1;   // first chunk of a piece: reset the state, load q
 constexpr int kLast = 2;    // last chunk of a piece: merge and write
@@ -227,6 +231,11 @@ struct DecodeSmem {
   alignas(8) uint64_t gen_full;
   // Table rows of the slice's sequences (when they fit).
   int slice_tab[kSliceTable];
+  int slice_slot[kSliceSlots];  // fused store: their slots
+  // Fused store: the new token's K and V rows of the stage's KV head, copied
+  // in with the chunk that holds the token.
+  alignas(16) __nv_bfloat16 knew[kStages][D];
+  alignas(16) __nv_bfloat16 vnew[kStages][D];
   // Cascade decode: fold scratch of the merger and of the merge warp.
   FoldScratch<G> fold_merger;
   FoldScratch<G> fold_merge;
@@ -556,6 +565,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       const int32_t* src = a.block_tables + static_cast<int64_t>(tab_seq0) * a.max_blocks;
       for (int i = lane; i < n; i += 32) sm.slice_tab[i] = __ldg(src + i);
     }
+    // Fused store: the slice's sequences' slots, likewise.
+    const bool fused = a.slot_mapping != nullptr;
+    const bool slot_smem = fused && tab_seq0 >= 0 && sm.end_seq >= tab_seq0 &&
+                           sm.end_seq - tab_seq0 + 1 <= kSliceSlots;
+    if (slot_smem)
+      for (int i = lane; i <= sm.end_seq - tab_seq0; i += 32)
+        sm.slice_slot[i] = __ldg(a.slot_mapping + tab_seq0 + i);
     __syncwarp();
     if (lane == 0) {
       // Last post of each stage (copies or descriptor only): phases of one
@@ -616,13 +632,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           inf.c_first = c_first;
           inf.c_last = c_last;
           inf.first_slot = first_slot;
+          inf.store_slot = -1;
+          inf.store_row = 0;
+          const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
+          if (fused && k == pnch - 1) {
+            // The pair's last chunk holds the new token (position ctx - 1).
+            const int want = slot_smem ? sm.slice_slot[pseq - tab_seq0] : a.slot_mapping[pseq];
+            if (inf.n_valid > 0 && want == slot_row + inf.n_valid - 1) {
+              inf.store_slot = want;
+              inf.store_row = inf.n_valid - 1;
+            } else if (want != -1) {
+              report_error(a.err, kErrDeviceCheck, kSiteDecodeStoreSlot);
+            }
+          }
           const uint32_t fb = smem_u32(&sm.full[st]);
           last_posted[st] = c;
           if (inf.n_valid <= 0) {
             mbar_arrive(fb);  // descriptor only
           } else {
-            const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
-            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u));
+            constexpr uint32_t kRowBytes = D * 2;
+            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u) +
+                                          (inf.store_slot >= 0 ? 2 * kRowBytes : 0u));
 #pragma unroll
             for (int pn = 0; pn < kPanels; ++pn) {
               tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
@@ -634,6 +664,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                             static_cast<int64_t>(pseq) * a.q_row_stride +
                             static_cast<int64_t>(kvh) * G * D,
                         kQBytes, fb);
+            if (inf.store_slot >= 0) {
+              bulk_load(smem_u32(&sm.knew[st][0]),
+                        static_cast<const __nv_bfloat16*>(a.k_new) +
+                            static_cast<int64_t>(pseq) * a.k_new_stride +
+                            static_cast<int64_t>(kvh) * D,
+                        kRowBytes, fb);
+              bulk_load(smem_u32(&sm.vnew[st][0]),
+                        static_cast<const __nv_bfloat16*>(a.v_new) +
+                            static_cast<int64_t>(pseq) * a.v_new_stride +
+                            static_cast<int64_t>(kvh) * D,
+                        kRowBytes, fb);
+            }
           }
         }
         return true;
@@ -789,6 +831,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             const int rest = i / kPanels;
             *reinterpret_cast<uint4*>(&sm.v[st][pn][(valid + rest / 8) * 128 + (rest % 8) * 16]) =
                 make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+          zeroed = true;
+        }
+        if (inf.store_slot >= 0) {
+          // Fused store: the new token's K and V rows of this KV head replace
+          // the pool rows loaded for its position, and are written to the
+          // cache slot (each pair stores its own head; one 16-byte piece per
+          // lane).
+          constexpr int kPieces = D / 8;
+          if (lane < 2 * kPieces) {
+            const bool is_v = lane >= kPieces;
+            const int ci = is_v ? lane - kPieces : lane;
+            const uint4 x =
+                *reinterpret_cast<const uint4*>((is_v ? sm.vnew[st] : sm.knew[st]) + ci * 8);
+            uint8_t* tile = is_v ? &sm.v[st][ci / 8][0] : &sm.k[st][ci / 8][0];
+            *reinterpret_cast<uint4*>(tile + sw128_offset(inf.store_row, ci % 8)) = x;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.v_cache : a.k_cache) +
+                                 static_cast<int64_t>(inf.store_slot) * a.num_kv_heads * D +
+                                 static_cast<int64_t>(inf.kvh) * D + ci * 8;
+            *reinterpret_cast<uint4*>(dst) = x;
           }
           __syncwarp();
           zeroed = true;

@@ -510,6 +510,70 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
       timed_launch("decode", s, [&] { return pkv::launch_decode(a, m, s); }));
 }
 
+pkv_status pkv_decode_attention_append(const void* q, int64_t q_row_stride, const void* k_new,
+                                       const void* v_new, int64_t k_row_stride,
+                                       int64_t v_row_stride, const int32_t* slot_mapping,
+                                       void* k_cache, void* v_cache, int64_t num_blocks,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, float scale, void* out,
+                                       pkv_stream_t stream) {
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_cache, v_cache, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  if (num_seqs > 0 && (!k_new || !v_new || !slot_mapping)) return PKV_ERR_INVALID_ARG;
+  const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (k_row_stride < row || v_row_stride < row) return PKV_ERR_INVALID_ARG;
+  if ((k_row_stride * 2) % 16 || (v_row_stride * 2) % 16) return PKV_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_UNSUPPORTED;
+  pkv::DecodeArgs a{};
+  const CacheMaps* maps = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0) return PKV_OK;
+    maps = cache_maps(ds, k_cache, v_cache, num_blocks, num_kv_heads, head_dim);
+    if (!maps) return PKV_ERR_CUDA;
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
+    a.err = ds->err;
+    const int g = num_q_heads / num_kv_heads;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    a.num_ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
+                          pkv::decode_counter_bytes(pairs));
+    if (st != PKV_OK) return st;
+    a.counters = ds->cnt;
+    a.part_o = ds->ws;
+    a.part_ml = a.part_o + static_cast<size_t>(a.num_ctas) * 2 * g * head_dim;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_new_stride = k_row_stride;
+    a.v_new_stride = v_row_stride;
+    a.slot_mapping = slot_mapping;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CacheMaps m = *maps;
+  return cuda_status(
+      timed_launch("decode_append", s, [&] { return pkv::launch_decode(a, m, s); }));
+}
+
 pkv_status pkv_decode_attention_shared_prefix(
     const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
     int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks_per_seq,

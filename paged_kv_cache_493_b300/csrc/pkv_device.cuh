@@ -27,6 +27,7 @@ enum ErrSite : int {
   kSiteDecodeWaitEmpty = 211,
   kSiteDecodeWaitMerge = 212,
   kSiteDecodeShared = 213,
+  kSiteDecodeStoreSlot = 214,
   kSiteDecodeI8Context = 220,
   kSiteDecodeI8Block = 221,
   kSitePrefillChunk = 300,

@@ -69,6 +69,20 @@ struct DecodeArgs {
   int shared_rows_pad;
   const float* shared_o;
   const float* shared_ml;
+  // Fused store (pkv_decode_attention_append; slot_mapping == nullptr: off):
+  // row s of k_new / v_new is sequence s's new token, the one at position
+  // context_lens[s] - 1.  The block that streams that position's chunk of
+  // pair (s, h) writes head h of the row into the cache at slot_mapping[s]
+  // and uses it in place of the pool row it loaded.  A slot of -1 stores
+  // nothing; any other slot than the position's is rejected (reported, not
+  // stored).
+  const void* k_new;
+  const void* v_new;
+  int64_t k_new_stride;  // elements
+  int64_t v_new_stride;
+  const int32_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
 };
 
 // Most units (key ranges) the shared prefix of a cascade decode is cut into.
