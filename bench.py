@@ -619,9 +619,9 @@ def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
     case = W.qwen_decode(seed=replica_seed(1002, rank))
     c = case.cache
     nb, bs, hkv, d = (int(x) for x in c.k_cache.shape)
-    kc = torch.empty((nb, bs, hkv, d), dtype=torch.int8, device="cuda")
+    kc = torch.empty((nb, hkv, bs, d), dtype=torch.int8, device="cuda")  # head-major blocks
     vc = torch.empty_like(kc)
-    ks = torch.empty((nb, bs, hkv), dtype=torch.float32, device="cuda")
+    ks = torch.empty((nb, hkv, bs), dtype=torch.float32, device="cuda")
     vs = torch.empty_like(ks)
     kb, vb = to_dev(c.k_cache).view(nb * bs, hkv, d), to_dev(c.v_cache).view(nb * bs, hkv, d)
     every = torch.arange(nb * bs, dtype=torch.int32, device="cuda")
@@ -653,7 +653,7 @@ def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
             "decode_bytes": dec_bytes, "decode_gbs": round(gbs, 2),
             "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
             "tokens_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1),
-            "kernels": "store_kvcache_int8; decode_int8 = split + combine"}
+            "kernels": "store_kvcache_int8; decode_int8 = the split-K decode kernel over codes"}
 
 
 def host_block_manager(pkv, steps: int = 2000) -> dict:

@@ -310,9 +310,12 @@ const char* pkv_version(void);
  * with IEEE binary32 division (codes in [-127, 127]; an all-zero row has
  * scale 0); a code stands for code * scale.  (The pages give no formula:
  * this is symmetric absmax quantisation per row.)
- *   k_codes, v_codes    int8 [num_blocks][256][num_kv_heads][head_dim]
- *   k_scales, v_scales  float32 [num_blocks][256][num_kv_heads]
- * all device pointers, 16-byte aligned, owned by the caller.
+ *   k_codes, v_codes    int8 [num_blocks][num_kv_heads][256][head_dim]
+ *   k_scales, v_scales  float32 [num_blocks][num_kv_heads][256]
+ * all device pointers, 16-byte aligned, owned by the caller.  Each block
+ * holds its KV heads one after another (the row of token slot
+ * s = block * 256 + offset and head h is (block * num_kv_heads + h) * 256 +
+ * offset), so a run of one head's tokens is contiguous.
  *
  * pkv_store_kvcache_int8 -- as pkv_store_kvcache (same k, v, strides and
  * slot_mapping rules, slot -1 skipped, out-of-range slots skipped and
@@ -330,12 +333,13 @@ pkv_status pkv_store_kvcache_int8(const void* k, const void* v, int64_t k_row_st
  * pkv_decode_attention_int8 -- pkv_decode_attention over an INT8 cache: the
  * same arguments, with the bf16 cache replaced by codes and scales, and the
  * same result on the values the codes stand for (fp32 accumulation, bf16
- * output).  A split-K kernel (512-token splits of each context, the G query
- * heads of a KV head together) followed by a log-sum-exp combine kernel;
- * the partial states live in the library's decode workspace (allocated on
- * first need), so overlapping calls on different streams must be
- * serialised by the caller.  Out-of-range block ids or context lengths give
- * a zero output for the sequence and PKV_ERR_DEVICE_CHECK.
+ * output).  The split-K decode kernel of pkv_decode_attention (same
+ * stream-K plan, in-kernel log-sum-exp merge, same workspace and the same
+ * rules for CUDA graphs and overlapping calls) reading 32-token tiles of
+ * codes and their scales; the codes become exact f16 values in registers,
+ * the K scale multiplies each score and the V scale each probability.  Out-
+ * of-range block ids or context lengths give a zero output for the sequence
+ * and PKV_ERR_DEVICE_CHECK.
  */
 pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const int8_t* k_codes,
                                      const int8_t* v_codes, const float* k_scales,

@@ -182,8 +182,9 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
 
 
 # ---------------------------------------------------------------------------
-# INT8 KV cache: codes int8 [num_blocks, 256, Hkv, D], scales float32
-# [num_blocks, 256, Hkv]; a value is code * scale.
+# INT8 KV cache: codes int8 [num_blocks, Hkv, 256, D], scales float32
+# [num_blocks, Hkv, 256] (each block holds its KV heads one after another);
+# a value is code * scale.
 # ---------------------------------------------------------------------------
 
 def quantize_rows(x: torch.Tensor) -> Tuple[np.ndarray, np.ndarray]:
@@ -196,10 +197,19 @@ def quantize_rows(x: torch.Tensor) -> Tuple[np.ndarray, np.ndarray]:
     return codes.reshape(tuple(x.shape)), scales.reshape(tuple(x.shape[:-1]))
 
 
+def quantize_pool(cache: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A bf16 pool [NB, 256, Hkv, D] as an INT8 pool holding the same tokens:
+    (codes int8 [NB, Hkv, 256, D], scales float32 [NB, Hkv, 256]) -- every
+    row quantised, then laid out head-major within each block."""
+    codes, scales = quantize_rows(cache)
+    return (torch.from_numpy(codes).transpose(1, 2).contiguous(),
+            torch.from_numpy(scales).transpose(1, 2).contiguous())
+
+
 def store_kvcache_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping, k_codes, v_codes,
                        k_scales, v_scales):
     """Returns new (k_codes, v_codes, k_scales, v_scales) CPU tensors; inputs unchanged."""
-    nb, bs, hkv, d = k_codes.shape
+    nb, hkv, bs, d = k_codes.shape
     kc, vc = k_codes.clone().contiguous(), v_codes.clone().contiguous()
     ks, vs = k_scales.clone().contiguous(), v_scales.clone().contiguous()
     kb, vb, sm = _bits(k), _bits(v), _i32(slot_mapping)
@@ -211,7 +221,7 @@ def store_kvcache_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping, k_codes, 
 
 def gather_int8(k_codes, v_codes, k_scales, v_scales, block_table_row,
                 context_len: int) -> Tuple[np.ndarray, np.ndarray]:
-    nb, bs, hkv, d = k_codes.shape
+    nb, hkv, bs, d = k_codes.shape
     row = _i32(block_table_row)
     n = max(int(context_len), 1)
     K = np.zeros((n, hkv, d), dtype=np.float64)
@@ -229,7 +239,7 @@ def decode_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tab
                 rows: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
     """Decode over an INT8 cache: full [B, Hq, D] output, or [len(rows), D]."""
     b, hq, d = q.shape
-    nb, bs, hkv, d2 = k_codes.shape
+    nb, hkv, bs, d2 = k_codes.shape
     assert d == d2 and k_codes.dtype == torch.int8 and k_scales.dtype == torch.float32
     bt, cl = _i32(block_tables), _i32(context_lens)
     if rows is None:

@@ -131,7 +131,7 @@ def decode_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tab
                 context_lens, scale: float, workers: Optional[int] = None) -> np.ndarray:
     """Full [B, Hq, D] output of ``oracle.decode_int8``, one task per sequence."""
     b, hq, d = q.shape
-    hkv = int(k_codes.shape[2])
+    hkv = int(k_codes.shape[1])  # codes [NB, Hkv, 256, D]
     bt = torch.as_tensor(block_tables, dtype=torch.int32).contiguous()
     cl = torch.as_tensor(context_lens, dtype=torch.int32).contiguous()
     out = np.zeros((b, hq, d), dtype=np.float64)

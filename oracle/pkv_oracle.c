@@ -131,9 +131,20 @@ void oracle_quantize_rows(const uint16_t* x, int64_t n_rows, int32_t n, int8_t* 
 }
 
 /*
+ * Where the INT8 cache keeps the row of (slot, KV head h): the pages fix no
+ * layout; each block holds its heads one after another, codes
+ * [num_blocks][num_kv_heads][256][head_dim] and scales
+ * [num_blocks][num_kv_heads][256], so row index
+ * (block * num_kv_heads + h) * 256 + offset, slot = block * 256 + offset.
+ */
+static int64_t int8_row(int64_t slot, int32_t num_kv_heads, int32_t h) {
+  return ((slot / ORACLE_BLOCK) * num_kv_heads + h) * ORACLE_BLOCK + slot % ORACLE_BLOCK;
+}
+
+/*
  * INT8 store: row i of k and v, head h, is quantised into cache slot
- * slot_mapping[i]: codes at k_codes[slot][h][:] and its scale at
- * k_scales[slot][h] (the same for v); slot -1 skips the row.
+ * slot_mapping[i]: codes at row int8_row(slot, h) of k_codes and its scale
+ * at the same index of k_scales (the same for v); slot -1 skips the row.
  */
 int oracle_store_kvcache_int8(const uint16_t* k, const uint16_t* v, int64_t k_row_stride,
                               int64_t v_row_stride, const int32_t* slot_mapping,
@@ -148,7 +159,7 @@ int oracle_store_kvcache_int8(const uint16_t* k, const uint16_t* v, int64_t k_ro
     if (slot == -1) continue;
     if (slot < 0 || slot >= num_slots) return ORACLE_BAD_SLOT;
     for (int32_t h = 0; h < num_kv_heads; ++h) {
-      const int64_t r = slot * num_kv_heads + h;
+      const int64_t r = int8_row(slot, num_kv_heads, h);
       oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,
                           k_codes + r * head_dim, k_scales + r);
       oracle_quantize_row(v + i * v_row_stride + (int64_t)h * head_dim, head_dim,
@@ -183,7 +194,7 @@ int oracle_gather(const uint16_t* k_cache, const uint16_t* v_cache, int64_t num_
 
 /*
  * Gather of an INT8 cache: as oracle_gather, each value being
- * code * scale of its (slot, KV head) row (exact in double).
+ * code * scale of its (slot, KV head) row int8_row(slot, h) (exact in double).
  */
 int oracle_gather_int8(const int8_t* k_codes, const int8_t* v_codes, const float* k_scales,
                        const float* v_scales, int64_t num_blocks, int32_t num_kv_heads,
@@ -197,7 +208,7 @@ int oracle_gather_int8(const int8_t* k_codes, const int8_t* v_codes, const float
     if (block < 0 || block >= num_blocks) return ORACLE_BAD_BLOCK;
     const int64_t slot = block * ORACLE_BLOCK + t % ORACLE_BLOCK;
     for (int32_t h = 0; h < num_kv_heads; ++h) {
-      const int64_t r = slot * num_kv_heads + h;
+      const int64_t r = int8_row(slot, num_kv_heads, h);
       const double ks = (double)k_scales[r], vs = (double)v_scales[r];
       for (int32_t d = 0; d < head_dim; ++d) {
         K[(int64_t)t * row + (int64_t)h * head_dim + d] = (double)k_codes[r * head_dim + d] * ks;
@@ -353,8 +364,8 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
                      num_q_heads, num_kv_heads, head_dim, scale, rows, n_rows, out);
 }
 
-/* Decode over an INT8 cache (codes [num_blocks][256][Hkv][D], scales
- * [num_blocks][256][Hkv]): the same attention on the values the codes stand for. */
+/* Decode over an INT8 cache (codes [num_blocks][Hkv][256][D], scales
+ * [num_blocks][Hkv][256]): the same attention on the values the codes stand for. */
 int oracle_decode_int8(const uint16_t* q, const int8_t* k_codes, const int8_t* v_codes,
                        const float* k_scales, const float* v_scales, int64_t num_blocks,
                        const int32_t* block_tables, int32_t max_blocks,

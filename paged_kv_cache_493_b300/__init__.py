@@ -274,15 +274,17 @@ def pkv_prefill_attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, conte
 
 
 def _int8_cache(k_codes, v_codes, k_scales, v_scales):
+    """INT8 cache: codes int8 [NB, Hkv, 256, D] and scales float32 [NB, Hkv, 256]
+    (each block holds its KV heads one after another)."""
     import torch
     for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
         _need(t.is_cuda and t.dtype == torch.int8 and t.dim() == 4 and t.is_contiguous()
-              and t.shape[1] == BLOCK_SIZE, f"{n}: contiguous int8 CUDA [NB, 256, Hkv, D]")
+              and t.shape[2] == BLOCK_SIZE, f"{n}: contiguous int8 CUDA [NB, Hkv, 256, D]")
     for t, n in ((k_scales, "k_scales"), (v_scales, "v_scales")):
         _need(t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
-              and tuple(t.shape) == tuple(k_codes.shape[:3]), f"{n}: contiguous float32 CUDA [NB, 256, Hkv]")
+              and tuple(t.shape) == tuple(k_codes.shape[:3]), f"{n}: contiguous float32 CUDA [NB, Hkv, 256]")
     _need(k_codes.shape == v_codes.shape, "k_codes and v_codes shapes differ")
-    nb, _, hkv, d = k_codes.shape
+    nb, hkv, _, d = k_codes.shape
     return int(nb), int(hkv), int(d)
 
 

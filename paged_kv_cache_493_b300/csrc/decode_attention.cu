@@ -74,7 +74,10 @@ namespace pkv {
 
 namespace {
 
-constexpr int kStages = 4;
+// Ring stages: 4 of 16 KB (K + V of a bf16 chunk at D = 128); INT8 chunks are
+// half the bytes, so 8 stages keep as many bytes in flight.
+template <bool kI8>
+constexpr int kStagesOf = kI8 ? 8 : 4;
 constexpr int kConsumerWarps = 4;  // warps 0..3: warp w computes the chunks c with c % 4 == w
 constexpr int kProducerWarp = 4;   // TMA issue
 constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
@@ -196,13 +199,64 @@ __device__ __forceinline__ const float* shared_o_at(const DecodeArgs& a, int seq
           static_cast<int64_t>(seq) * G + h) * D + d;
 }
 
+// The ring's K/V tiles.  bf16: per stage, D / 64 panels of 32 rows x 128
+// bytes (128-byte swizzle).  INT8: per stage, 32 rows x D bytes of codes
+// (128-byte swizzle for D = 128, 64-byte for D = 64) and the 32 tokens'
+// scales of the stage's KV head.
+template <int D, bool kI8>
+struct KvTiles {
+  uint8_t k[kStagesOf<false>][D / 64][kPanelBytes];
+  uint8_t v[kStagesOf<false>][D / 64][kPanelBytes];
+};
+template <int D>
+struct KvTiles<D, true> {
+  uint8_t k[kStagesOf<true>][kDecodeChunk * D];
+  uint8_t v[kStagesOf<true>][kDecodeChunk * D];
+  alignas(16) float ks[kStagesOf<true>][kDecodeChunk];
+  alignas(16) float vs[kStagesOf<true>][kDecodeChunk];
+};
+
+// Byte offset of 16-byte piece `chunk` of row `row` in a TMA tile of D-byte
+// int8 rows: 128-byte swizzle for D = 128 (the piece index XOR row % 8),
+// 64-byte swizzle for D = 64 (XOR (row / 2) % 4).
+template <int D>
+__device__ __forceinline__ uint32_t i8_offset(int row, int chunk) {
+  if constexpr (D == 128) return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+  else return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+// INT8 codes as exact f16 values.  With x = codes XOR 0x80808080 (each byte
+// biased to u = code + 128), the f16 with bits 0x64uu is 1024 + u, and
+// subtracting 1152 (0x6480) leaves the code; both steps are exact.  One byte
+// permute and one packed subtraction per pair.
+constexpr uint32_t kF16Magic = 0x64646464u;
+constexpr uint32_t kF16Bias = 0x64806480u;
+// Bytes 0, 1 of x as an f16 pair (lo = byte 0).
+__device__ __forceinline__ uint32_t i8_b01_f16x2(uint32_t x) {
+  return sub_f16x2(__byte_perm(x, kF16Magic, 0x4140), kF16Bias);
+}
+// Bytes 2, 3 of x as an f16 pair (lo = byte 2).
+__device__ __forceinline__ uint32_t i8_b23_f16x2(uint32_t x) {
+  return sub_f16x2(__byte_perm(x, kF16Magic, 0x4342), kF16Bias);
+}
+// The f16 pairs (byte e of xa, byte e of xb) for e = 0, 1 (lo01) and
+// e = 2, 3 (hi23): one interleaving permute per two pairs.
+__device__ __forceinline__ void i8_cross_f16x2(uint32_t xa, uint32_t xb, uint32_t (&e01)[2],
+                                               uint32_t (&e23)[2]) {
+  const uint32_t t01 = __byte_perm(xa, xb, 0x5140);  // a0 b0 a1 b1
+  const uint32_t t23 = __byte_perm(xa, xb, 0x7362);  // a2 b2 a3 b3
+  e01[0] = i8_b01_f16x2(t01);
+  e01[1] = i8_b23_f16x2(t01);
+  e23[0] = i8_b01_f16x2(t23);
+  e23[1] = i8_b23_f16x2(t23);
+}
+
 // Placed at a 1024-byte-aligned address (the 128-byte swizzle repeats every
 // 1024 bytes and the panels must start on that boundary).
-template <int D, int G>
-struct DecodeSmem {
+template <int D, int G, bool kI8 = false>
+struct DecodeSmem : KvTiles<D, kI8> {
   static constexpr int kPanels = D / 64;
-  uint8_t k[kStages][kPanels][kPanelBytes];
-  uint8_t v[kStages][kPanels][kPanelBytes];
+  static constexpr int kStages = kStagesOf<kI8>;
   alignas(16) __nv_bfloat16 q[kStages][G * D];
   // Mailbox from the consumer warps to the merger: each warp's state of a
   // finished piece.
@@ -241,10 +295,14 @@ struct DecodeSmem {
   FoldScratch<G> fold_merge;
 };
 
-template <int D, int G>
+template <int D, int G, bool kI8 = false>
 constexpr size_t decode_smem_bytes() {
-  return sizeof(DecodeSmem<D, G>) + 1024;  // slack for the 1024-byte alignment
+  return sizeof(DecodeSmem<D, G, kI8>) + 1024;  // slack for the 1024-byte alignment
 }
+// Two blocks per SM (228 KB of shared memory, 1 KB reserved per block) for
+// the group sizes up to 8 (bf16) and 4 (INT8, whose ring is twice as deep).
+static_assert(decode_smem_bytes<128, 8, false>() <= 113 * 1024, "bf16 decode: 2 blocks per SM");
+static_assert(decode_smem_bytes<128, 4, true>() <= 113 * 1024, "INT8 decode: 2 blocks per SM");
 
 // A context this kernel rejects: out of range, or (cascade decode) shorter
 // than the shared prefix.
@@ -453,19 +511,23 @@ constexpr int decode_max_regs() {
   return G <= 8 ? 128 : 255;
 }
 
-template <int D, int G>
+// kI8 = false: bf16 cache (kmap / vmap over the bf16 pools).  kI8 = true:
+// INT8 cache (kmap / vmap over the int8 codes, box {D bytes, 1, 32}; the
+// scales a.k_scales / a.v_scales come in by plain bulk copies).
+template <int D, int G, bool kI8>
 __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<G>())
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
   constexpr int kPanels = D / 64;
-  constexpr uint32_t kChunkBytes = kDecodeChunk * D * 2;
+  constexpr int kStages = kStagesOf<kI8>;
+  constexpr uint32_t kChunkBytes = kDecodeChunk * D * (kI8 ? 1 : 2);
   constexpr uint32_t kQBytes = G * D * 2;
   constexpr int kWarps = kDecodeThreads / 32;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t sraw = smem_u32(smem_raw);
-  DecodeSmem<D, G>& sm =
-      *reinterpret_cast<DecodeSmem<D, G>*>(smem_raw + (((sraw + 1023u) & ~1023u) - sraw));
+  DecodeSmem<D, G, kI8>& sm =
+      *reinterpret_cast<DecodeSmem<D, G, kI8>*>(smem_raw + (((sraw + 1023u) & ~1023u) - sraw));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -651,12 +713,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             mbar_arrive(fb);  // descriptor only
           } else {
             constexpr uint32_t kRowBytes = D * 2;
-            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + (k == k0 ? kQBytes : 0u) +
+            constexpr uint32_t kScaleBytes = kI8 ? kDecodeChunk * 4 : 0u;
+            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + 2 * kScaleBytes +
+                                          (k == k0 ? kQBytes : 0u) +
                                           (inf.store_slot >= 0 ? 2 * kRowBytes : 0u));
+            if constexpr (kI8) {
+              // Head-major INT8 blocks: the chunk's codes of this KV head are
+              // one contiguous 32 x D tile (rows of (block, head) = id * Hkv
+              // + kvh), and its 32 scales 128 contiguous bytes.
+              const int bh = id * a.num_kv_heads + kvh;
+              tma_load_3d(smem_u32(&sm.k[st][0]), &kmap, fb, 0, tok & (kBlockSize - 1), bh);
+              tma_load_3d(smem_u32(&sm.v[st][0]), &vmap, fb, 0, tok & (kBlockSize - 1), bh);
+              const int64_t srow =
+                  static_cast<int64_t>(bh) * kBlockSize + (tok & (kBlockSize - 1));
+              bulk_load(smem_u32(&sm.ks[st][0]), a.k_scales + srow, kScaleBytes, fb);
+              bulk_load(smem_u32(&sm.vs[st][0]), a.v_scales + srow, kScaleBytes, fb);
+            } else {
 #pragma unroll
-            for (int pn = 0; pn < kPanels; ++pn) {
-              tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
-              tma_load_3d(smem_u32(&sm.v[st][pn][0]), &vmap, fb, pn * 64, kvh, slot_row);
+              for (int pn = 0; pn < kPanels; ++pn) {
+                tma_load_3d(smem_u32(&sm.k[st][pn][0]), &kmap, fb, pn * 64, kvh, slot_row);
+                tma_load_3d(smem_u32(&sm.v[st][pn][0]), &vmap, fb, pn * 64, kvh, slot_row);
+              }
             }
             if (k == k0)
               bulk_load(smem_u32(&sm.q[st][0]),
@@ -755,6 +832,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     float m_run[NT][2];      // running max of heads nt*8 + 2cq + j (log2 domain)
     float l_run[NT][2];      // this lane's share of their running sums
     bool piece_bad = false;
+    // INT8 (f16 operands): q of head h is scaled by a power of two so that
+    // max |q| lies in [1/2, 1) (exact, then rounded to f16); qmul undoes it for
+    // the scores of heads nt*8 + 2cq + j.  P is multiplied by vscale_t /
+    // vs_ref, vs_ref the running maximum of the piece's V scales (so P <= 1
+    // in f16), and the accumulator is scaled by vs_ref when posted.
+    float qmul[NT][2];
+    float vs_ref = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) qmul[nt][0] = qmul[nt][1] = 0.f;
 #pragma unroll
     for (int md = 0; md < KS; ++md)
 #pragma unroll
@@ -810,51 +896,94 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             const int h = nt * 8 + g;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-              const __nv_bfloat16* qr = &sm.q[st][h * D + ks * 16 + 2 * cq];
+              // The k index of the MMA runs over head dimensions: bf16 keys
+              // use them in order; INT8 keys are read four bytes (four
+              // dimensions) per lane, so logical k 2cq, 2cq+1 | 2cq+8, 2cq+9
+              // of step ks stand for dimensions 16 ks + 4 cq + 0, 1 | 2, 3.
+              const __nv_bfloat16* qr = kI8 ? &sm.q[st][h * D + ks * 16 + 4 * cq]
+                                            : &sm.q[st][h * D + ks * 16 + 2 * cq];
               qb[ks][nt][0] = h < G ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
-              qb[ks][nt][1] = h < G ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+              qb[ks][nt][1] = h < G ? *reinterpret_cast<const uint32_t*>(qr + (kI8 ? 2 : 8)) : 0u;
+            }
+            if constexpr (kI8) {
+              // max |q| of head h over the four lanes of row group g
+              float amax = 0.f;
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2)
+                  amax = fmax3(amax, fabsf(bf16_lo(qb[ks][nt][k2])), fabsf(bf16_hi(qb[ks][nt][k2])));
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+              // 2^-(E+1) and 2^(E+1) for amax = m 2^E, 1 <= m < 2
+              const uint32_t eb = min((__float_as_uint(amax) >> 23) & 0xFFu, 252u);
+              const float down = amax > 0.f ? __uint_as_float((253u - eb) << 23) : 1.f;
+              const float up = amax > 0.f ? __uint_as_float((eb + 1u) << 23) : 0.f;
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2)
+                  qb[ks][nt][k2] = pack_f16x2(bf16_lo(qb[ks][nt][k2]) * down,
+                                              bf16_hi(qb[ks][nt][k2]) * down);
+#pragma unroll
+              for (int j = 0; j < 2; ++j)
+                qmul[nt][j] = __shfl_sync(0xffffffffu, up, (2 * cq + j) * 4);
             }
           }
         }
+        vs_ref = 0.f;
       }
       piece_bad |= (inf.flags & kBad) != 0;
       const int valid = inf.n_valid;
       bool zeroed = false;
       if ((c % kConsumerWarps) == warp && valid > 0) {
-        const uint32_t kb = smem_u32(&sm.k[st][0][0]);
-        const uint32_t vb = smem_u32(&sm.v[st][0][0]);
-        if (valid < kDecodeChunk) {
-          // V rows past the context: zero them (pool contents may be
-          // anything, and 0 x NaN would poison the product).
-          for (int i = lane; i < (kDecodeChunk - valid) * 8 * kPanels; i += 32) {
-            const int pn = i % kPanels;
-            const int rest = i / kPanels;
-            *reinterpret_cast<uint4*>(&sm.v[st][pn][(valid + rest / 8) * 128 + (rest % 8) * 16]) =
-                make_uint4(0u, 0u, 0u, 0u);
+        // INT8: the K and V scales of this lane's four tokens (mt * 16 +
+        // hf * 8 + g); read for tokens past the context too, but always
+        // selected away there (pool contents may be anything).
+        float ksc[2][2], vsc[2][2];
+        if constexpr (kI8) {
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int tok = mt * 16 + hf * 8 + g;
+              ksc[mt][hf] = sm.ks[st][tok];
+              vsc[mt][hf] = sm.vs[st][tok];
+            }
+        } else {
+          if (valid < kDecodeChunk) {
+            // V rows past the context: zero them (pool contents may be
+            // anything, and 0 x NaN would poison the product).
+            for (int i = lane; i < (kDecodeChunk - valid) * 8 * kPanels; i += 32) {
+              const int pn = i % kPanels;
+              const int rest = i / kPanels;
+              *reinterpret_cast<uint4*>(&sm.v[st][pn][(valid + rest / 8) * 128 + (rest % 8) * 16]) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+            zeroed = true;
           }
-          __syncwarp();
-          zeroed = true;
-        }
-        if (inf.store_slot >= 0) {
-          // Fused store: the new token's K and V rows of this KV head replace
-          // the pool rows loaded for its position, and are written to the
-          // cache slot (each pair stores its own head; one 16-byte piece per
-          // lane).
-          constexpr int kPieces = D / 8;
-          if (lane < 2 * kPieces) {
-            const bool is_v = lane >= kPieces;
-            const int ci = is_v ? lane - kPieces : lane;
-            const uint4 x =
-                *reinterpret_cast<const uint4*>((is_v ? sm.vnew[st] : sm.knew[st]) + ci * 8);
-            uint8_t* tile = is_v ? &sm.v[st][ci / 8][0] : &sm.k[st][ci / 8][0];
-            *reinterpret_cast<uint4*>(tile + sw128_offset(inf.store_row, ci % 8)) = x;
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.v_cache : a.k_cache) +
-                                 static_cast<int64_t>(inf.store_slot) * a.num_kv_heads * D +
-                                 static_cast<int64_t>(inf.kvh) * D + ci * 8;
-            *reinterpret_cast<uint4*>(dst) = x;
+          if (inf.store_slot >= 0) {
+            // Fused store: the new token's K and V rows of this KV head replace
+            // the pool rows loaded for its position, and are written to the
+            // cache slot (each pair stores its own head; one 16-byte piece per
+            // lane).
+            constexpr int kPieces = D / 8;
+            if (lane < 2 * kPieces) {
+              const bool is_v = lane >= kPieces;
+              const int ci = is_v ? lane - kPieces : lane;
+              const uint4 x =
+                  *reinterpret_cast<const uint4*>((is_v ? sm.vnew[st] : sm.knew[st]) + ci * 8);
+              uint8_t* tile = is_v ? &sm.v[st][ci / 8][0] : &sm.k[st][ci / 8][0];
+              *reinterpret_cast<uint4*>(tile + sw128_offset(inf.store_row, ci % 8)) = x;
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.v_cache : a.k_cache) +
+                                   static_cast<int64_t>(inf.store_slot) * a.num_kv_heads * D +
+                                   static_cast<int64_t>(inf.kvh) * D + ci * 8;
+              *reinterpret_cast<uint4*>(dst) = x;
+            }
+            __syncwarp();
+            zeroed = true;
           }
-          __syncwarp();
-          zeroed = true;
         }
         // ---- S^T = K q^T: two m-tiles of 16 tokens x NT n-tiles of 8 heads
         float sc[2][NT][4];
@@ -864,17 +993,68 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+        if constexpr (kI8) {
+          // Codes converted to bf16 exactly in registers: lane (g, cq) reads
+          // four bytes (dimensions 16 ks + 4 cq .. + 3) of token rows g and
+          // g + 8 of each m-tile (conflict-free under the swizzle).
+          const uint8_t* k8 = sm.k[st];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+          for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            uint32_t af[4];
-            ldsm_x4(kb + (ks >> 2) * kPanelBytes +
-                        sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
-                    af);
+            for (int mt = 0; mt < 2; ++mt) {
+              const int r0 = mt * 16 + g;
+              const uint32_t w0 =
+                  *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0, ks) + 4 * cq) ^
+                  0x80808080u;
+              const uint32_t w1 =
+                  *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0 + 8, ks) + 4 * cq) ^
+                  0x80808080u;
+              uint32_t af[4];
+              af[0] = i8_b01_f16x2(w0);
+              af[2] = i8_b23_f16x2(w0);
+              af[1] = i8_b01_f16x2(w1);
+              af[3] = i8_b23_f16x2(w1);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
+              for (int nt = 0; nt < NT; ++nt)
+                mma_16816_f16(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
+            }
           }
+        } else {
+          const uint32_t kb = smem_u32(&sm.k[st][0][0]);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+              uint32_t af[4];
+              ldsm_x4(kb + (ks >> 2) * kPanelBytes +
+                          sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
+                      af);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_16816(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
+            }
+          }
+        }
+        // INT8: the running maximum of the piece's V scales (valid tokens;
+        // the eight row groups hold the chunk's tokens).  When it grows the
+        // accumulator, kept in units of it, is rescaled with the softmax's
+        // alpha below.
+        float vfix = 1.f, inv_vs = 0.f;
+        if constexpr (kI8) {
+          float cm = 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              if (mt * 16 + hf * 8 + g < valid) cm = fmaxf(cm, vsc[mt][hf]);
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+          if (cm > vs_ref) {
+            vfix = vs_ref / cm;
+            vs_ref = cm;
+          }
+          inv_vs = vs_ref > 0.f ? 1.f / vs_ref : 0.f;
         }
         // ---- online softmax per head (a head's 32 scores sit in the lanes
         // with the same cq: two per m-tile in each of the 8 row groups)
@@ -889,7 +1069,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 const int tok = mt * 16 + hf * 8 + g;
-                const float x = tok < valid ? sc[mt][nt][hf * 2 + j] * qscale : -INFINITY;
+                const float sx = kI8 ? qscale * ksc[mt][hf] * qmul[nt][j] : qscale;
+                const float x = tok < valid ? sc[mt][nt][hf * 2 + j] * sx : -INFINITY;
                 sc[mt][nt][hf * 2 + j] = x;
                 mx = fmaxf(mx, x);
               }
@@ -905,10 +1086,15 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 const float pv = fast_exp2(sc[mt][nt][hf * 2 + j] - m_new);
-                sc[mt][nt][hf * 2 + j] = pv;
                 ls += pv;
+                // INT8: P V = vs_ref sum_t (p_t vscale_t / vs_ref) code_t,
+                // with p_t vscale_t / vs_ref <= 1 in f16; the sum keeps p_t.
+                const int tok = mt * 16 + hf * 8 + g;
+                sc[mt][nt][hf * 2 + j] =
+                    kI8 ? (tok < valid ? pv * (vsc[mt][hf] * inv_vs) : 0.f) : pv;
               }
             l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + ls;
+            if constexpr (kI8) alpha[nt][j] *= vfix;
           }
         }
 #pragma unroll
@@ -921,27 +1107,72 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             o[md][nt][3] *= alpha[nt][1];
           }
         // ---- P^T operand fragments: the S^T accumulator of tokens
-        // mt*16 + (0..7 | 8..15) is an 8x8 bf16 matrix per lane pair of
-        // columns; its transpose is the operand layout.
+        // mt*16 + (0..7 | 8..15) is an 8x8 16-bit matrix per lane pair of
+        // columns; its transpose is the operand layout (bf16, or f16 for
+        // INT8).
         uint32_t pb[2][NT][2];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            pb[mt][nt][0] = movmatrix_trans(pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
-            pb[mt][nt][1] = movmatrix_trans(pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
+            pb[mt][nt][0] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][0], sc[mt][nt][1])
+                                                : pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
+            pb[mt][nt][1] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][2], sc[mt][nt][3])
+                                                : pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
           }
         // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, two k-steps of 16 tokens
+        if constexpr (kI8) {
+          // Lane (g, cq) reads four bytes (dimensions 4 (g + 8 p) .. + 3) of
+          // token rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 of the k-step and
+          // pairs the tokens per dimension; dimension 4 (g + 8 p) + e is row
+          // g + 8 (e & 1) of m-tile 2 p + (e >> 1) (the output rows are put
+          // back in order when the state is posted).
+          const uint8_t* v8 = sm.v[st];
 #pragma unroll
-        for (int kt = 0; kt < 2; ++kt) {
+          for (int kt = 0; kt < 2; ++kt) {
+            const int t0 = kt * 16 + 2 * cq;
 #pragma unroll
-          for (int md = 0; md < KS; ++md) {
-            uint32_t af[4];
-            ldsm_x4_trans(vb + (md >> 2) * kPanelBytes +
-                              sw128_offset(kt * 16 + (li >> 1) * 8 + lr, (md & 3) * 2 + (li & 1)),
-                          af);
+            for (int p = 0; p < D / 32; ++p) {
+              const int ch = (g >> 2) + 2 * p;
+              const int wo = 4 * (g & 3);
+              const uint32_t x0 =
+                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0, ch) + wo) ^ 0x80808080u;
+              const uint32_t x1 =
+                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 1, ch) + wo) ^
+                  0x80808080u;
+              const uint32_t x2 =
+                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 8, ch) + wo) ^
+                  0x80808080u;
+              const uint32_t x3 =
+                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 9, ch) + wo) ^
+                  0x80808080u;
+              // Token pairs (t0, t0 + 1) and (t0 + 8, t0 + 9) per byte e.
+              uint32_t lo01[2], lo23[2], hi01[2], hi23[2];
+              i8_cross_f16x2(x0, x1, lo01, lo23);
+              i8_cross_f16x2(x2, x3, hi01, hi23);
+              const uint32_t af0[4] = {lo01[0], lo01[1], hi01[0], hi01[1]};  // e = 0, 1
+              const uint32_t af1[4] = {lo23[0], lo23[1], hi23[0], hi23[1]};  // e = 2, 3
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(o[md][nt], af, pb[kt][nt][0], pb[kt][nt][1]);
+              for (int nt = 0; nt < NT; ++nt) {
+                mma_16816_f16(o[2 * p][nt], af0, pb[kt][nt][0], pb[kt][nt][1]);
+                mma_16816_f16(o[2 * p + 1][nt], af1, pb[kt][nt][0], pb[kt][nt][1]);
+              }
+            }
+          }
+        } else {
+          const uint32_t vb = smem_u32(&sm.v[st][0][0]);
+#pragma unroll
+          for (int kt = 0; kt < 2; ++kt) {
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+              uint32_t af[4];
+              ldsm_x4_trans(vb + (md >> 2) * kPanelBytes +
+                                sw128_offset(kt * 16 + (li >> 1) * 8 + lr, (md & 3) * 2 + (li & 1)),
+                            af);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma_16816(o[md][nt], af, pb[kt][nt][0], pb[kt][nt][1]);
+            }
           }
         }
       }
@@ -978,7 +1209,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int h = nt * 8 + 2 * cq + (e & 1);
-              if (h < G) sm.mail_o[warp][h][md * 16 + g + (e >> 1) * 8] = o[md][nt][e];
+              // Dimension of accumulator row g + 8 (e >> 1) of m-tile md.
+              const int dim = kI8 ? 4 * (g + 8 * (md >> 1)) + (md & 1) * 2 + (e >> 1)
+                                  : md * 16 + g + (e >> 1) * 8;
+              if (h < G) sm.mail_o[warp][h][dim] = kI8 ? o[md][nt][e] * vs_ref : o[md][nt][e];
             }
         if (warp == 0 && lane == 0) {  // every warp saw the same descriptors
           StageInfo post = inf;
@@ -1186,15 +1420,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-template <int D, int G>
+template <int D, int G, bool kI8>
 int ctas_per_sm() {
   static int per_sm = 0;
   if (per_sm == 0) {
-    const size_t smem = decode_smem_bytes<D, G>();
-    auto kern = decode_split_kernel<D, G>;
+    const size_t smem = decode_smem_bytes<D, G, kI8>();
+    auto kern = decode_split_kernel<D, G, kI8>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kDecodeThreads, smem) !=
             cudaSuccess) {
       cudaGetLastError();
@@ -1205,23 +1441,27 @@ int ctas_per_sm() {
   return per_sm;
 }
 
-template <int D>
+template <int D, bool kI8>
 int ctas_per_sm_d(int group) {
   switch (group) {
-    case 1: return ctas_per_sm<D, 1>();
-    case 2: return ctas_per_sm<D, 2>();
-    case 4: return ctas_per_sm<D, 4>();
-    case 8: return ctas_per_sm<D, 8>();
-    default: return ctas_per_sm<D, 16>();
+    case 1: return ctas_per_sm<D, 1, kI8>();
+    case 2: return ctas_per_sm<D, 2, kI8>();
+    case 4: return ctas_per_sm<D, 4, kI8>();
+    case 8: return ctas_per_sm<D, 8, kI8>();
+    default: return ctas_per_sm<D, 16, kI8>();
   }
 }
 
-template <int D, int G>
-cudaError_t launch_split_t(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream) {
-  const size_t smem = decode_smem_bytes<D, G>();
-  auto kern = decode_split_kernel<D, G>;
+template <int D, int G, bool kI8>
+cudaError_t launch_split_t(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream) {
+  const size_t smem = decode_smem_bytes<D, G, kI8>();
+  auto kern = decode_split_kernel<D, G, kI8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (a.num_ctas <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -1234,25 +1474,30 @@ cudaError_t launch_split_t(const DecodeArgs& a, const CacheMaps& maps, cudaStrea
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, maps.k_rows, maps.v_rows, a);
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, a);
 }
 
-template <int D>
-cudaError_t launch_split_d(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream) {
+template <int D, bool kI8>
+cudaError_t launch_split_d(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           cudaStream_t stream) {
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_split_t<D, 1>(a, maps, stream);
-    case 2: return launch_split_t<D, 2>(a, maps, stream);
-    case 4: return launch_split_t<D, 4>(a, maps, stream);
-    case 8: return launch_split_t<D, 8>(a, maps, stream);
-    case 16: return launch_split_t<D, 16>(a, maps, stream);
+    case 1: return launch_split_t<D, 1, kI8>(a, kmap, vmap, stream);
+    case 2: return launch_split_t<D, 2, kI8>(a, kmap, vmap, stream);
+    case 4: return launch_split_t<D, 4, kI8>(a, kmap, vmap, stream);
+    case 8: return launch_split_t<D, 8, kI8>(a, kmap, vmap, stream);
+    case 16: return launch_split_t<D, 16, kI8>(a, kmap, vmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int max_splits) {
-  const int per_sm = head_dim == 64 ? ctas_per_sm_d<64>(group) : ctas_per_sm_d<128>(group);
+int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int max_splits,
+                    bool int8) {
+  const int per_sm = int8 ? (head_dim == 64 ? ctas_per_sm_d<64, true>(group)
+                                            : ctas_per_sm_d<128, true>(group))
+                          : (head_dim == 64 ? ctas_per_sm_d<64, false>(group)
+                                            : ctas_per_sm_d<128, false>(group));
   int64_t n = static_cast<int64_t>(per_sm) * (num_sms > 0 ? num_sms : 1);
   if (max_splits > 0 && num_pairs * max_splits < n) n = num_pairs * max_splits;
   if (n < 1) n = 1;
@@ -1269,8 +1514,16 @@ size_t decode_partial_bytes(int num_ctas, int group, int head_dim) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream) {
-  if (a.head_dim == 128) return launch_split_d<128>(a, maps, stream);
-  if (a.head_dim == 64) return launch_split_d<64>(a, maps, stream);
+  if (a.head_dim == 128) return launch_split_d<128, false>(a, maps.k_rows, maps.v_rows, stream);
+  if (a.head_dim == 64) return launch_split_d<64, false>(a, maps.k_rows, maps.v_rows, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_i8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream) {
+  if (!a.k_scales || !a.v_scales) return cudaErrorInvalidValue;
+  if (a.head_dim == 128) return launch_split_d<128, true>(a, kmap, vmap, stream);
+  if (a.head_dim == 64) return launch_split_d<64, true>(a, kmap, vmap, stream);
   return cudaErrorInvalidValue;
 }
 

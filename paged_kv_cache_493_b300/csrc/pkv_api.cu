@@ -158,14 +158,31 @@ DeviceState* device_state(pkv_status* st) {
 
 bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1,
-               uint32_t b2, CUtensorMapSwizzle swz) {
+               uint32_t b2, CUtensorMapSwizzle swz,
+               CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   const cuuint64_t dims[3] = {d0, d1, d2};
   const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
   const cuuint32_t box[3] = {b0, b1, b2};
   const cuuint32_t elem[3] = {1, 1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps over INT8 codes [num_blocks][Hkv][256][D] bytes viewed as 3-D
+// {D, 256, num_blocks * Hkv} for the decode: box {D, 32, 1} (32 consecutive
+// tokens of one (block, KV head), one contiguous tile), 128-byte swizzle for
+// D = 128 and 64-byte for D = 64 (the swizzle span is the row).
+bool encode_int8_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k, const void* v,
+                      int64_t num_blocks, int hkv, int d) {
+  const uint64_t tiles = static_cast<uint64_t>(num_blocks) * hkv;
+  const uint64_t blk = pkv::kBlockSize;
+  const CUtensorMapSwizzle swz =
+      d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return encode_3d(kmap, k, d, blk, tiles, d, blk * d, d, pkv::kDecodeChunk, 1, swz,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
+         encode_3d(vmap, v, d, blk, tiles, d, blk * d, d, pkv::kDecodeChunk, 1, swz,
+                   CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
 // Tensor maps over the cache viewed as [slots][Hkv][D] (3-D: D, Hkv, slots).
@@ -423,24 +440,19 @@ pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const 
   if (st != PKV_OK) return st;
   if (!k_scales || !v_scales) return PKV_ERR_INVALID_ARG;
   if (!aligned16(k_scales) || !aligned16(v_scales)) return PKV_ERR_UNSUPPORTED;
-  pkv::DecodeI8Args a{};
+  // The split-K decode kernel over the codes (TMA ring, tensor cores, the
+  // same stream-K plan and in-kernel merge as the bf16 decode).
+  pkv::DecodeArgs a{};
+  CUtensorMap kmap, vmap;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceState* ds = device_state(&st);
     if (!ds) return st;
     if (num_seqs == 0) return PKV_OK;
-    a.splits = pkv::decode_int8_splits(max_blocks_per_seq);
-    st = ensure_workspace(ds,
-                          pkv::decode_int8_partial_bytes(num_seqs, num_kv_heads, a.splits,
-                                                         num_q_heads / num_kv_heads, head_dim),
-                          0);
-    if (st != PKV_OK) return st;
+    if (!encode_int8_maps(&kmap, &vmap, k_codes, v_codes, num_blocks, num_kv_heads, head_dim))
+      return PKV_ERR_CUDA;
     a.q = q;
     a.q_row_stride = q_row_stride;
-    a.k_codes = k_codes;
-    a.v_codes = v_codes;
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
     a.block_tables = block_tables;
     a.max_blocks = max_blocks_per_seq;
     a.context_lens = context_lens;
@@ -451,12 +463,24 @@ pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const 
     a.num_blocks = num_blocks;
     a.scale = scale;
     a.out = out;
-    a.part = ds->ws;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
     a.err = ds->err;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    const int g = num_q_heads / num_kv_heads;
+    const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
+    a.num_ctas =
+        pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load(), true);
+    st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
+                          pkv::decode_counter_bytes(pairs));
+    if (st != PKV_OK) return st;
+    a.counters = ds->cnt;
+    a.part_o = ds->ws;
+    a.part_ml = a.part_o + static_cast<size_t>(a.num_ctas) * 2 * g * head_dim;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return cuda_status(
-      timed_launch("decode_int8", s, [&] { return pkv::launch_decode_int8(a, s); }));
+      timed_launch("decode_int8", s, [&] { return pkv::launch_decode_i8(a, kmap, vmap, s); }));
 }
 
 pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void* k_cache,
@@ -772,12 +796,12 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
     // whole table width.
     shared = std::max(shared, shared_plan(std::max(num_seqs, 1), num_q_heads / g, g, head_dim,
                                           max_blocks_per_seq, ds->num_sms).bytes);
-    const int ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
-    part = std::max(part, pkv::decode_partial_bytes(ctas, g, head_dim));
-    // The INT8 decode keeps its split partials in the same workspace.
-    part = std::max(part, pkv::decode_int8_partial_bytes(num_seqs, num_q_heads / g,
-                                                         pkv::decode_int8_splits(max_blocks_per_seq),
-                                                         g, head_dim));
+    // The bf16 and INT8 decodes (their grids may differ) share the workspace.
+    for (const bool int8 : {false, true}) {
+      const int ctas =
+          pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load(), int8);
+      part = std::max(part, pkv::decode_partial_bytes(ctas, g, head_dim));
+    }
     cnt = std::max(cnt, pkv::decode_counter_bytes(pairs));
   }
   const pkv_status st2 = ensure_workspace(ds, part, cnt);

@@ -83,6 +83,10 @@ struct DecodeArgs {
   const int32_t* slot_mapping;
   void* k_cache;
   void* v_cache;
+  // INT8 cache (launch_decode_i8): the fp32 scales [slots][Hkv] of the codes
+  // the tensor maps cover.
+  const float* k_scales;
+  const float* v_scales;
 };
 
 // Most units (key ranges) the shared prefix of a cascade decode is cut into.
@@ -138,31 +142,6 @@ struct StoreI8Args {
   DeviceError* err;
 };
 
-struct DecodeI8Args {
-  const void* q;
-  int64_t q_row_stride;  // elements
-  const int8_t* k_codes;
-  const int8_t* v_codes;
-  const float* k_scales;
-  const float* v_scales;
-  const int32_t* block_tables;
-  int max_blocks;
-  const int32_t* context_lens;
-  int num_seqs;
-  int num_q_heads;
-  int num_kv_heads;
-  int head_dim;
-  int64_t num_blocks;
-  float scale;
-  void* out;
-  int splits;   // token splits per (sequence, KV head): ceil(max_blocks * 256 / kInt8SplitTokens)
-  float* part;  // [num_seqs][num_kv_heads][splits][G][head_dim + 2]
-  DeviceError* err;
-};
-
-// Tokens per split of the INT8 decode.
-constexpr int kInt8SplitTokens = 512;
-
 // Tensor maps built by the API layer (cached per cache pointer).
 struct CacheMaps {
   CUtensorMap k_rows;   // decode: box {64, 1, 32} over [slots][Hkv][D], 128-byte swizzle
@@ -178,20 +157,21 @@ constexpr int kPrefillKeyTile = 64;
 
 cudaError_t launch_store_kvcache(const StoreArgs& a, cudaStream_t stream);
 cudaError_t launch_store_kvcache_int8(const StoreI8Args& a, cudaStream_t stream);
-// Splits of the INT8 decode for a table width, and the bytes of its partials.
-int decode_int8_splits(int max_blocks);
-size_t decode_int8_partial_bytes(int64_t num_seqs, int num_kv_heads, int splits, int group,
-                                 int head_dim);
-cudaError_t launch_decode_int8(const DecodeI8Args& a, cudaStream_t stream);
 
 // Blocks of the decode kernel for a batch: as many as fit on the GPU at
 // once, at most num_pairs * max_splits when max_splits > 0.
-int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int max_splits);
+int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int max_splits,
+                    bool int8 = false);
 // Bytes of the decode kernel's arrival counters (zero when first used) and of
 // its partial slots.
 size_t decode_counter_bytes(int64_t num_pairs);
 size_t decode_partial_bytes(int num_ctas, int group, int head_dim);
 cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream);
+// The same split-K decode over an INT8 cache: kmap / vmap view the codes as
+// uint8 {D, Hkv, slots} with box {D, 1, 32} (128-byte swizzle for D = 128,
+// 64-byte for D = 64); a.k_scales / a.v_scales are set.  At most 8 KV heads.
+cudaError_t launch_decode_i8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                             cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream);

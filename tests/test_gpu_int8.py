@@ -22,10 +22,11 @@ def default_knobs():
 
 
 def int8_pool(cache):
-    """The INT8 cache holding the same tokens as a bf16 pool (CPU tensors)."""
-    kc, ks = oracle.quantize_rows(cache.k_cache)
-    vc, vs = oracle.quantize_rows(cache.v_cache)
-    return [torch.from_numpy(a) for a in (kc, vc, ks, vs)]
+    """The INT8 cache holding the same tokens as a bf16 pool (CPU tensors:
+    codes [NB, Hkv, 256, D], scales [NB, Hkv, 256])."""
+    kc, ks = oracle.quantize_pool(cache.k_cache)
+    vc, vs = oracle.quantize_pool(cache.v_cache)
+    return [kc, vc, ks, vs]
 
 
 def tie_rows(n, hkv, d):
@@ -46,9 +47,9 @@ def test_store_int8_codes_and_scales_are_exact(cuda_device, d):
     v[20:30] = 0                                   # zero rows: scale 0, codes 0
     slots = torch.randperm(nb * 256, generator=g)[:n].to(torch.int32)
     slots[::7] = -1
-    kc = torch.randint(-127, 128, (nb, 256, hkv, d), generator=g, dtype=torch.int8)
+    kc = torch.randint(-127, 128, (nb, hkv, 256, d), generator=g, dtype=torch.int8)
     vc = kc.clone()
-    ks = torch.rand(nb, 256, hkv, generator=g)
+    ks = torch.rand(nb, hkv, 256, generator=g)
     vs = ks.clone()
     want = oracle.store_kvcache_int8(k, v, slots, kc, vc, ks, vs)
     got = [dev(t) for t in (kc, vc, ks, vs)]
@@ -110,10 +111,50 @@ def test_int8_geometries(cuda_device, d, hq, hkv):
     check_case(case)
 
 
-def test_int8_long_contexts_sampled(cuda_device):
+def test_int8_long_contexts(cuda_device):
     case = W.make_decode_case("long8", [9000, 4097, 31], 16, 8, 128, 64, seed=77)
-    rows = [(s, h) for s in range(3) for h in range(16)]
-    check_case(case, rows)
+    check_case(case)
+
+
+@pytest.mark.parametrize("cap", [1, 3])
+def test_int8_split_cap_does_not_change_result(cuda_device, cap):
+    case = W.make_decode_case("cap8", [1, 300, 1500, 4000], 16, 8, 128, 40, seed=78, k_scale=3.0)
+    pkv.pkv_set_max_splits(cap)
+    try:
+        check_case(case)
+    finally:
+        pkv.pkv_set_max_splits(0)
+
+
+def test_int8_many_kv_heads(cuda_device):
+    """32 KV heads (one query head each), head_dim 64: each head's tiles and
+    scales are its own contiguous runs of the block."""
+    case = W.make_decode_case("h32", [5, 300, 700], 32, 32, 64, 12, seed=79)
+    check_case(case)
+
+
+def test_int8_graph_replays_follow_new_inputs(cuda_device):
+    case = W.qwen_decode(seed=1047, num_seqs=24)
+    c = case.cache
+    pool = int8_pool(c)
+    kc, vc, ks, vs = [dev(t) for t in pool]
+    bt, cl = dev(c.block_tables), dev(c.context_lens)
+    q = dev(case.q)
+    out = torch.empty_like(q)
+    pkv.pkv_reserve_workspace(24, 16, 128, int(bt.shape[1]))
+    pkv.pkv_decode_attention_int8(q, kc, vc, ks, vs, bt, cl, case.scale, out)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pkv.pkv_decode_attention_int8(q, kc, vc, ks, vs, bt, cl, case.scale, out)
+    for seed in (1, 2):
+        newq = W.randn_bf16(tuple(case.q.shape), torch.Generator().manual_seed(seed))
+        q.copy_(dev(newq))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.decode_int8(newq, *pool, c.block_tables, c.context_lens, case.scale)
+        assert_close(out, ref, f"replay {seed}")
+    no_device_error()
 
 
 def test_int8_bad_block_and_context_give_zeros(cuda_device):

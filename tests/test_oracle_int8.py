@@ -65,11 +65,12 @@ def test_round_to_nearest_bound_and_range(d):
 
 
 def int8_cache_of(case):
-    """Quantise a case's bf16 pools row by row (the INT8 cache holding the same tokens)."""
+    """Quantise a case's bf16 pools row by row (the INT8 cache holding the same
+    tokens, codes [NB, Hkv, 256, D], scales [NB, Hkv, 256])."""
     c = case.cache
-    kc, ks = oracle.quantize_rows(c.k_cache)
-    vc, vs = oracle.quantize_rows(c.v_cache)
-    return (torch.from_numpy(kc), torch.from_numpy(vc), torch.from_numpy(ks), torch.from_numpy(vs))
+    kc, ks = oracle.quantize_pool(c.k_cache)
+    vc, vs = oracle.quantize_pool(c.v_cache)
+    return kc, vc, ks, vs
 
 
 def test_gather_recovers_rows_within_half_a_step():
@@ -84,7 +85,7 @@ def test_gather_recovers_rows_within_half_a_step():
             step = np.zeros(got.shape[:2])
             for t in range(ctx):
                 blk = int(c.block_tables[s, t // 256])
-                step[t] = sc[blk, t % 256].numpy()
+                step[t] = sc[blk, :, t % 256].numpy()
             assert np.all(np.abs(got - ref) <= step[:, :, None] * (0.5 + 127 * 2.0 ** -24))
 
 
@@ -127,19 +128,19 @@ def test_store_int8_writes_quantised_rows_and_skips_minus_one():
     g = torch.Generator().manual_seed(3)
     k = torch.randn(3, hkv, d, generator=g).to(torch.bfloat16)
     v = torch.randn(3, hkv, d, generator=g).to(torch.bfloat16)
-    kc = torch.full((nb, 256, hkv, d), 5, dtype=torch.int8)
+    kc = torch.full((nb, hkv, 256, d), 5, dtype=torch.int8)  # head-major blocks
     vc = kc.clone()
-    ks = torch.full((nb, 256, hkv), 9.0)
+    ks = torch.full((nb, hkv, 256), 9.0)
     vs = ks.clone()
     nkc, nvc, nks, nvs = oracle.store_kvcache_int8(k, v, [5, -1, 258], kc, vc, ks, vs)
     qk, sk = oracle.quantize_rows(k)
     qv, sv = oracle.quantize_rows(v)
     for i, slot in ((0, 5), (2, 258)):
         b, o = divmod(slot, 256)
-        assert np.array_equal(nkc[b, o].numpy(), qk[i]) and np.array_equal(nvc[b, o].numpy(), qv[i])
-        assert np.array_equal(nks[b, o].numpy(), sk[i]) and np.array_equal(nvs[b, o].numpy(), sv[i])
-    untouched = torch.ones(nb, 256, dtype=torch.bool)
-    untouched[0, 5] = untouched[1, 2] = False
+        assert np.array_equal(nkc[b, :, o].numpy(), qk[i]) and np.array_equal(nvc[b, :, o].numpy(), qv[i])
+        assert np.array_equal(nks[b, :, o].numpy(), sk[i]) and np.array_equal(nvs[b, :, o].numpy(), sv[i])
+    untouched = torch.ones(nb, hkv, 256, dtype=torch.bool)
+    untouched[0, :, 5] = untouched[1, :, 2] = False
     assert torch.all(nkc[untouched] == 5) and torch.all(nks[untouched] == 9.0)
     with pytest.raises(oracle.OracleError):
         oracle.store_kvcache_int8(k, v, [5, -2, 258], kc, vc, ks, vs)
@@ -165,6 +166,8 @@ MUTANTS = {
                              "oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,"),
     "store_head_offset_dropped": ("oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,",
                                   "oracle_quantize_row(k + i * k_row_stride, head_dim,"),
+    "slot_major_rows": ("return ((slot / ORACLE_BLOCK) * num_kv_heads + h) * ORACLE_BLOCK + slot % ORACLE_BLOCK;",
+                        "return slot * num_kv_heads + h;"),
 }
 
 PINS = [

@@ -32,9 +32,8 @@ def test_parallel_prefill_equals_serial():
 def test_parallel_decode_int8_equals_serial():
     case = W.make_decode_case("p", [5, 260, 90], 4, 2, 64, 8, seed=33)
     c = case.cache
-    kc, ks = oracle.quantize_rows(c.k_cache)
-    vc, vs = oracle.quantize_rows(c.v_cache)
-    kc, vc, ks, vs = (torch.from_numpy(x) for x in (kc, vc, ks, vs))
+    kc, ks = oracle.quantize_pool(c.k_cache)
+    vc, vs = oracle.quantize_pool(c.v_cache)
     ref = oracle.decode_int8(case.q, kc, vc, ks, vs, c.block_tables, c.context_lens, case.scale)
     got = parallel.decode_int8(case.q, kc, vc, ks, vs, c.block_tables, c.context_lens,
                                case.scale, workers=3)
