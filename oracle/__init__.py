@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_gather_int8.argtypes = [P, P, P, P, I64, I32, I32, P, I32, I32, P, P]
         _lib.oracle_decode_int8.argtypes = [P, P, P, P, P, I64, P, I32, P, I32, I32, I32, I32, D,
                                             P, I32, P]
+        _lib.oracle_prefill_int8.argtypes = [P, P, P, P, P, I64, P, I32, P, P, I32, I32, I32,
+                                             I32, D, P, I32, P]
     return _lib
 
 
@@ -255,4 +257,30 @@ def decode_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tab
     _check(lib().oracle_decode_int8(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb,
                                     _ptr(bt), int(bt.shape[1]), _ptr(cl), b, hq, hkv, d,
                                     float(scale), rptr, nr, _ptr(out)))
+    return out
+
+
+def prefill_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tables,
+                 cu_seqlens_q, context_lens, scale: float,
+                 rows: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """Chunked prefill over an INT8 cache: full [T, Hq, D] output, or
+    [len(rows), D] for (token row, q head) pairs."""
+    t, hq, d = q.shape
+    nb, hkv, bs, d2 = k_codes.shape
+    assert d == d2 and k_codes.dtype == torch.int8 and k_scales.dtype == torch.float32
+    bt, cu, cl = _i32(block_tables), _i32(cu_seqlens_q), _i32(context_lens)
+    if rows is None:
+        out = np.zeros((t, hq, d), dtype=np.float64)
+        rptr, nr = None, 0
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros((r.shape[0], d), dtype=np.float64)
+        rptr, nr = _ptr(r), r.shape[0]
+    kc, vc = k_codes.contiguous(), v_codes.contiguous()
+    ks, vs = k_scales.contiguous(), v_scales.contiguous()
+    qb = _bits(q)
+    _check(lib().oracle_prefill_int8(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), nb,
+                                     _ptr(bt), int(bt.shape[1]), _ptr(cu), _ptr(cl),
+                                     int(cu.numel() - 1), hq, hkv, d, float(scale), rptr, nr,
+                                     _ptr(out)))
     return out

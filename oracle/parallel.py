@@ -5,7 +5,8 @@ the benchmark's CPU-baseline legs, never by the library.
 
 Nothing here computes attention.  The work is cut into independent tasks --
 one sequence, or one sequence and a subset of its query heads -- and each
-task calls the unchanged ``oracle.decode`` / ``oracle.prefill`` on a slice of
+task calls the unchanged ``oracle`` function (decode, prefill or their INT8
+forms) on a slice of
 the inputs; the tasks run on a thread pool (ctypes releases the interpreter
 lock for the duration of each C call, so the threads run on separate cores).
 Outputs are placed back where the single-threaded call would have put them,
@@ -89,18 +90,15 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_
     return out
 
 
-def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables,
-            cu_seqlens_q, context_lens, scale: float, workers: Optional[int] = None,
-            head_groups: Optional[int] = None) -> np.ndarray:
-    """Full [T, Hq, D] output of ``oracle.prefill``, one task per (sequence,
-    group of query heads); ``head_groups`` defaults to enough groups to give
-    every thread a task."""
+def _prefill_tasks(call, q: torch.Tensor, hkv: int, block_tables, cu_seqlens_q, context_lens,
+                   workers: Optional[int], head_groups: Optional[int]) -> np.ndarray:
+    """Runs ``call(q_rows, bt_row, local_cu, cl_row, rows)`` -- one oracle
+    prefill over a single sequence -- for every (sequence, group of query
+    heads) task and assembles the full [T, Hq, D] output."""
     t, hq, d = q.shape
-    hkv = int(k_cache.shape[2])
     bt = torch.as_tensor(block_tables, dtype=torch.int32).contiguous()
     cu = torch.as_tensor(cu_seqlens_q, dtype=torch.int32).tolist()
     cl = torch.as_tensor(context_lens, dtype=torch.int32).contiguous()
-    k_cache, v_cache = k_cache.contiguous(), v_cache.contiguous()
     b = len(cu) - 1
     out = np.zeros((t, hq, d), dtype=np.float64)
     n_workers = pick_workers(_gather_bytes(max([int(x) for x in cl.tolist()] + [1]), hkv, d),
@@ -119,12 +117,41 @@ def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block
         heads = list(range(h0, min(h0 + per, hq)))
         rows = [(r, h) for r in range(t1 - t0) for h in heads]
         local_cu = torch.tensor([0, t1 - t0], dtype=torch.int32)
-        res = oracle.prefill(q[t0:t1], k_cache, v_cache, bt[s:s + 1], local_cu, cl[s:s + 1],
-                             scale, rows=rows)
+        res = call(q[t0:t1], bt[s:s + 1], local_cu, cl[s:s + 1], rows)
         out[t0:t1, h0:h0 + len(heads)] = res.reshape(t1 - t0, len(heads), d)
 
     _run(tasks, one, n_workers)
     return out
+
+
+def prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables,
+            cu_seqlens_q, context_lens, scale: float, workers: Optional[int] = None,
+            head_groups: Optional[int] = None) -> np.ndarray:
+    """Full [T, Hq, D] output of ``oracle.prefill``, one task per (sequence,
+    group of query heads); ``head_groups`` defaults to enough groups to give
+    every thread a task."""
+    k_cache, v_cache = k_cache.contiguous(), v_cache.contiguous()
+
+    def call(qs, bt, cu, cl, rows):
+        return oracle.prefill(qs, k_cache, v_cache, bt, cu, cl, scale, rows=rows)
+
+    return _prefill_tasks(call, q, int(k_cache.shape[2]), block_tables, cu_seqlens_q,
+                          context_lens, workers, head_groups)
+
+
+def prefill_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tables,
+                 cu_seqlens_q, context_lens, scale: float, workers: Optional[int] = None,
+                 head_groups: Optional[int] = None) -> np.ndarray:
+    """Full [T, Hq, D] output of ``oracle.prefill_int8``, split as ``prefill``."""
+    k_codes, v_codes = k_codes.contiguous(), v_codes.contiguous()
+    k_scales, v_scales = k_scales.contiguous(), v_scales.contiguous()
+
+    def call(qs, bt, cu, cl, rows):
+        return oracle.prefill_int8(qs, k_codes, v_codes, k_scales, v_scales, bt, cu, cl, scale,
+                                   rows=rows)
+
+    return _prefill_tasks(call, q, int(k_codes.shape[1]), block_tables, cu_seqlens_q,
+                          context_lens, workers, head_groups)
 
 
 def decode_int8(q: torch.Tensor, k_codes, v_codes, k_scales, v_scales, block_tables,

@@ -104,7 +104,13 @@ int oracle_store_kvcache(const uint16_t* k, const uint16_t* v, int64_t k_row_str
  *   scale = max_d |x_d| / 127,  code_d = nearest(x_d / scale), ties to even,
  * both decided in binary32 (the precision the codes are decided in on the
  * GPU too), codes in [-127, 127]; an all-zero row has scale 0 and zero
- * codes.  The value a code stands for is code * scale.
+ * codes.  The value a code stands for is code * scale.  Decode and prefill
+ * over the INT8 cache are the same attention as over the bf16 cache, on the
+ * gathered values code * scale (exact in double).  Pins
+ * (tests/test_oracle_int8.py): hand-worked quantised rows, the
+ * round-to-nearest bound, and, with integer rows (every scale 1), bit
+ * equality with the bf16 decode and prefill; the last row of an INT8 prefill
+ * chunk equals the INT8 decode of that query.
  */
 void oracle_quantize_row(const uint16_t* x, int32_t n, int8_t* codes, float* scale) {
   float amax = 0.0f;
@@ -387,11 +393,12 @@ int oracle_decode_int8(const uint16_t* q, const int8_t* k_codes, const int8_t* v
  * (token row, q head) pairs are computed into out[n_rows][head_dim];
  * otherwise out is [total][num_q_heads][head_dim].
  */
-int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
-                   int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
-                   const int32_t* cu_seqlens_q, const int32_t* context_lens, int32_t num_seqs,
-                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, double scale,
-                   const int32_t* rows, int32_t n_rows, double* out) {
+static int prefill_from(const uint16_t* q, const CacheSource* cache, int64_t num_blocks,
+                        const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, double scale, const int32_t* rows, int32_t n_rows,
+                        double* out) {
   int rc = check_heads(num_q_heads, num_kv_heads, head_dim);
   if (rc) return rc;
   const int32_t group = num_q_heads / num_kv_heads;
@@ -421,8 +428,8 @@ int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v
       rc = ORACLE_NO_MEMORY;
       break;
     }
-    rc = oracle_gather(k_cache, v_cache, num_blocks, num_kv_heads, head_dim,
-                       block_tables + (int64_t)s * max_blocks, max_blocks, ctx, K, V);
+    rc = gather_from(cache, num_blocks, num_kv_heads, head_dim,
+                     block_tables + (int64_t)s * max_blocks, max_blocks, ctx, K, V);
     for (int32_t tok = t0; tok < t1 && rc == ORACLE_OK; ++tok) {
       const int32_t n_keys = ctx - lq + (tok - t0) + 1;
       for (int32_t h = 0; h < num_q_heads; ++h) {
@@ -446,4 +453,28 @@ int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v
   }
   free(qrow);
   return rc;
+}
+
+int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                   int64_t num_blocks, const int32_t* block_tables, int32_t max_blocks,
+                   const int32_t* cu_seqlens_q, const int32_t* context_lens, int32_t num_seqs,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, double scale,
+                   const int32_t* rows, int32_t n_rows, double* out) {
+  const CacheSource c = {k_cache, v_cache, NULL, NULL, NULL, NULL};
+  return prefill_from(q, &c, num_blocks, block_tables, max_blocks, cu_seqlens_q, context_lens,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, scale, rows, n_rows, out);
+}
+
+/* Chunked prefill over an INT8 cache (layout as for oracle_decode_int8): the
+ * same causal attention on the values code * scale the codes stand for. */
+int oracle_prefill_int8(const uint16_t* q, const int8_t* k_codes, const int8_t* v_codes,
+                        const float* k_scales, const float* v_scales, int64_t num_blocks,
+                        const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                        int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, double scale, const int32_t* rows, int32_t n_rows,
+                        double* out) {
+  const CacheSource c = {NULL, NULL, k_codes, v_codes, k_scales, v_scales};
+  return prefill_from(q, &c, num_blocks, block_tables, max_blocks, cu_seqlens_q, context_lens,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, scale, rows, n_rows, out);
 }

@@ -112,6 +112,47 @@ def test_int8_decode_is_bf16_decode_when_quantisation_is_exact():
     assert np.array_equal(got, want)
 
 
+def integer_prefill_case(seed):
+    """A chunked-prefill case with the same integer K/V rows (every scale 1)."""
+    case = W.make_prefill_case("exact_p", [0, 37, 250, 300], [5, 30, 9, 40], 4, 2, 64, 8,
+                               seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    for t in (case.cache.k_cache, case.cache.v_cache):
+        ints = torch.randint(-126, 127, t.shape, generator=g).float()
+        ints[..., 0] = torch.where(torch.rand(t.shape[:-1], generator=g) < 0.5, 127.0, -127.0)
+        t.copy_(ints.to(torch.bfloat16))
+    case.q.copy_((case.q.float() / 64).to(torch.bfloat16))
+    return case
+
+
+def test_int8_prefill_is_bf16_prefill_when_quantisation_is_exact():
+    case = integer_prefill_case(9)
+    kc, vc, ks, vs = int8_cache_of(case)
+    assert torch.all(ks == 1) and torch.all(vs == 1)
+    c = case.cache
+    want = oracle.prefill(case.q, c.k_cache, c.v_cache, c.block_tables, case.cu_seqlens_q,
+                          c.context_lens, case.scale)
+    got = oracle.prefill_int8(case.q, kc, vc, ks, vs, c.block_tables, case.cu_seqlens_q,
+                              c.context_lens, case.scale)
+    assert np.array_equal(got, want)
+
+
+def test_int8_prefill_last_row_is_int8_decode():
+    """The last query of a chunk sees the whole context, as a decode query
+    does: on general (scaled) rows the two give the same numbers."""
+    case = W.make_prefill_case("last", [0, 37, 250, 300], [5, 30, 9, 40], 4, 2, 64, 8, seed=10)
+    kc, vc, ks, vs = int8_cache_of(case)
+    assert not torch.all(ks == 1)
+    c = case.cache
+    cu = case.cu_seqlens_q.tolist()
+    got = oracle.prefill_int8(case.q, kc, vc, ks, vs, c.block_tables, case.cu_seqlens_q,
+                              c.context_lens, case.scale)
+    last = torch.stack([case.q[cu[s + 1] - 1] for s in range(len(cu) - 1)])
+    dec = oracle.decode_int8(last, kc, vc, ks, vs, c.block_tables, c.context_lens, case.scale)
+    for s in range(len(cu) - 1):
+        assert np.array_equal(got[cu[s + 1] - 1], dec[s]), s
+
+
 def test_int8_decode_stays_close_to_bf16_decode():
     """Quantisation noise (relative 1/254 per element at worst) moves the
     attention output little: a sanity bound, not a tolerance of the kernels."""
@@ -166,6 +207,12 @@ MUTANTS = {
                              "oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,"),
     "store_head_offset_dropped": ("oracle_quantize_row(k + i * k_row_stride + (int64_t)h * head_dim, head_dim,",
                                   "oracle_quantize_row(k + i * k_row_stride, head_dim,"),
+    "prefill_int8_scales_swapped": (
+        "const CacheSource c = {NULL, NULL, k_codes, v_codes, k_scales, v_scales};\n  return prefill_from(",
+        "const CacheSource c = {NULL, NULL, k_codes, v_codes, v_scales, k_scales};\n  return prefill_from("),
+    "prefill_int8_codes_swapped": (
+        "const CacheSource c = {NULL, NULL, k_codes, v_codes, k_scales, v_scales};\n  return prefill_from(",
+        "const CacheSource c = {NULL, NULL, v_codes, k_codes, k_scales, v_scales};\n  return prefill_from("),
     "slot_major_rows": ("return ((slot / ORACLE_BLOCK) * num_kv_heads + h) * ORACLE_BLOCK + slot % ORACLE_BLOCK;",
                         "return slot * num_kv_heads + h;"),
 }
@@ -176,6 +223,8 @@ PINS = [
     test_gather_recovers_rows_within_half_a_step,
     test_int8_decode_is_bf16_decode_when_quantisation_is_exact,
     test_store_int8_writes_quantised_rows_and_skips_minus_one,
+    test_int8_prefill_is_bf16_prefill_when_quantisation_is_exact,
+    test_int8_prefill_last_row_is_int8_decode,
 ]
 
 

@@ -40,6 +40,19 @@ def test_parallel_decode_int8_equals_serial():
     assert np.array_equal(got, ref)
 
 
+def test_parallel_prefill_int8_equals_serial():
+    case = W.make_prefill_case("p", [300, 0, 17], [40, 33, 0], 8, 2, 64, 16, seed=34)
+    c = case.cache
+    kc, ks = oracle.quantize_pool(c.k_cache)
+    vc, vs = oracle.quantize_pool(c.v_cache)
+    ref = oracle.prefill_int8(case.q, kc, vc, ks, vs, c.block_tables, case.cu_seqlens_q,
+                              c.context_lens, case.scale)
+    for groups in (1, 4):
+        got = parallel.prefill_int8(case.q, kc, vc, ks, vs, c.block_tables, case.cu_seqlens_q,
+                                    c.context_lens, case.scale, workers=3, head_groups=groups)
+        assert np.array_equal(got, ref), groups
+
+
 def test_worker_count_respects_memory():
     assert parallel.pick_workers(0, workers=5) == 5
     assert parallel.pick_workers(1 << 62) == 1   # one task's buffers exceed the memory
