@@ -12,8 +12,9 @@ replayed, as a serving engine replays its decode step; the eager (uncaptured)
 time and the same step as two calls (pkv_store_kvcache, then
 pkv_decode_attention) are reported beside it.
 The metric is KV GB/s (algorithmic bytes / step time) with decode tokens/s per
-layer beside it.  The long-context decode, prefix-sharing decode and chunked
-prefill workloads are measured too and reported under "other_workloads", with
+layer beside it.  The long-context decode, prefix-sharing decode, chunked
+prefill and INT8-cache (decode and prefill) workloads are measured too and
+reported under "other_workloads", with
 the host cost of the block manager that produces the decode step's block
 tables and slot mapping.
 
@@ -566,6 +567,9 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
     if only is None or only == "qwen_decode_b128_int8":
         res["qwen_decode_b128_int8"] = int8_decode_workload(pkv, steps, flush, peaks, rank)
         torch.cuda.empty_cache()
+    if only is None or only == "chunked_prefill_8x512_int8":
+        res["chunked_prefill_8x512_int8"] = int8_prefill_workload(pkv, steps, flush, peaks, rank)
+        torch.cuda.empty_cache()
     if only is None:
         res["host_block_manager"] = host_block_manager(pkv)
     if only is not None and only != "chunked_prefill_8x512":
@@ -613,20 +617,12 @@ def other_workloads(pkv, args, rank, flush, peaks, only=None):
 
 def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
     """The 128-sequence decode step over the INT8 cache: quantising store of
-    the new rows, then decode (split + combine kernels).  The INT8 pool holds
-    the same tokens as the bf16 pool: the quantising store is run over every
-    slot of it first."""
+    the new rows, then the split-K decode over the codes.  The INT8 pool
+    holds the same tokens as the bf16 pool."""
     case = W.qwen_decode(seed=replica_seed(1002, rank))
     c = case.cache
     nb, bs, hkv, d = (int(x) for x in c.k_cache.shape)
-    kc = torch.empty((nb, hkv, bs, d), dtype=torch.int8, device="cuda")  # head-major blocks
-    vc = torch.empty_like(kc)
-    ks = torch.empty((nb, hkv, bs), dtype=torch.float32, device="cuda")
-    vs = torch.empty_like(ks)
-    kb, vb = to_dev(c.k_cache).view(nb * bs, hkv, d), to_dev(c.v_cache).view(nb * bs, hkv, d)
-    every = torch.arange(nb * bs, dtype=torch.int32, device="cuda")
-    pkv.pkv_store_kvcache_int8(kb, vb, every, kc, vc, ks, vs)
-    del kb, vb, every
+    kc, vc, ks, vs = int8_pool_of(c)
     q, kn, vn, sm = to_dev(case.q), to_dev(case.k_new), to_dev(case.v_new), to_dev(case.slot_mapping)
     bt, cl = to_dev(c.block_tables), to_dev(c.context_lens)
     out = torch.empty_like(q)
@@ -654,6 +650,58 @@ def int8_decode_workload(pkv, steps, flush, peaks, rank) -> dict:
             "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
             "tokens_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1),
             "kernels": "store_kvcache_int8; decode_int8 = the split-K decode kernel over codes"}
+
+
+def int8_pool_of(c):
+    """Device INT8 pool (codes [NB, Hkv, 256, D], scales [NB, Hkv, 256])
+    holding the same tokens as the case's bf16 pool: the quantising store is
+    run over every slot of it."""
+    nb, bs, hkv, d = (int(x) for x in c.k_cache.shape)
+    kc = torch.empty((nb, hkv, bs, d), dtype=torch.int8, device="cuda")
+    vc = torch.empty_like(kc)
+    ks = torch.empty((nb, hkv, bs), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    kb, vb = to_dev(c.k_cache).view(nb * bs, hkv, d), to_dev(c.v_cache).view(nb * bs, hkv, d)
+    every = torch.arange(nb * bs, dtype=torch.int32, device="cuda")
+    import paged_kv_cache_493_b300 as pkv
+    pkv.pkv_store_kvcache_int8(kb, vb, every, kc, vc, ks, vs)
+    torch.cuda.synchronize()
+    return kc, vc, ks, vs
+
+
+def int8_prefill_workload(pkv, steps, flush, peaks, rank) -> dict:
+    """The 8 x 512 chunked-prefill step over the INT8 cache: quantising
+    store of the chunk's rows, then the INT8 prefill (tiles dequantised to
+    bf16 in shared memory, then the tcgen05 pipeline)."""
+    case = W.chunked_prefill(seed=replica_seed(1005, rank))
+    c = case.cache
+    kc, vc, ks, vs = int8_pool_of(c)
+    bt, cl, cu = to_dev(c.block_tables), to_dev(c.context_lens), to_dev(case.cu_seqlens_q)
+    q, kn, vn, sm = to_dev(case.q), to_dev(case.k_new), to_dev(case.v_new), to_dev(case.slot_mapping)
+    out = torch.empty_like(q)
+
+    def step():
+        pkv.pkv_store_kvcache_int8(kn, vn, sm, kc, vc, ks, vs)
+        pkv.pkv_prefill_attention_int8(q, kc, vc, ks, vs, bt, cu, cl, case.scale, out)
+
+    def pcall():
+        pkv.pkv_prefill_attention_int8(q, kc, vc, ks, vs, bt, cu, cl, case.scale, out)
+
+    for _ in range(3):
+        step()
+    kt = kernel_times(pkv, step, steps, flush, ["store_kvcache_int8", "prefill_int8"])
+    per, _ = time_steps(capture_graph(step), steps, flush)
+    pper, _ = time_steps(capture_graph(pcall), steps, flush)
+    flops = prefill_flops(case)
+    pre_ms = sum(pper) / len(pper)
+    tf = flops / (pre_ms * 1e-3) / 1e12
+    return {"step_ms": round(sum(per) / len(per), 5), "prefill_ms": round(pre_ms, 5),
+            "flops": flops, "timing": "graph replays, L2 flushed before each",
+            "tflops": round(tf, 2), "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "frac_of_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+            "kernel_ms_eager": {n: round(v[0] / max(v[1], 1), 5) for n, v in kt.items()},
+            "kernels": "store_kvcache_int8; prefill_int8 = the tcgen05 prefill kernel with "
+                       "producer warps dequantising INT8 tiles to bf16 in shared memory"}
 
 
 def host_block_manager(pkv, steps: int = 2000) -> dict:
@@ -804,7 +852,8 @@ def main(argv=None):
     ap.add_argument("--only-main", action="store_true", help="skip the other workloads")
     ap.add_argument("--workload", default=MAIN_WORKLOAD,
                     choices=[MAIN_WORKLOAD, "long_decode_32k", "prefix_decode_b64",
-                             "chunked_prefill_8x512", "qwen_decode_b128_int8"],
+                             "chunked_prefill_8x512", "qwen_decode_b128_int8",
+                             "chunked_prefill_8x512_int8"],
                     help="run one non-default workload alone (for profiling) and print its entry")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "pkv":

@@ -350,6 +350,27 @@ pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const 
                                      float scale, void* out, pkv_stream_t stream);
 
 /*
+ * pkv_prefill_attention_int8 -- pkv_prefill_attention over an INT8 cache:
+ * the same arguments and chunk rules, with the bf16 cache replaced by codes
+ * and scales, and the same causal attention on the values the codes stand
+ * for (fp32 accumulation, bf16 output).  The tensor-core prefill kernel of
+ * pkv_prefill_attention; each 64-key tile of codes and its scales is
+ * loaded into shared memory and turned there into the bf16 values
+ * code * scale (rounded to nearest even) before the matrix products, so the
+ * result differs from the exact values only by that rounding, of the order
+ * of the bf16 cache's own.  Allocates nothing.  Bad chunk lengths or block
+ * ids give a zero output for the rows of the tile and PKV_ERR_DEVICE_CHECK.
+ */
+pkv_status pkv_prefill_attention_int8(const void* q, int64_t q_row_stride, const int8_t* k_codes,
+                                      const int8_t* v_codes, const float* k_scales,
+                                      const float* v_scales, int64_t num_blocks,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                      int32_t num_seqs, int64_t total_q, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, float scale,
+                                      void* out, pkv_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's error
  * word (a static device variable of the library, shared by every call on
  * that device; reading it allocates nothing).  *code receives PKV_OK or the first PKV_ERR_DEVICE_CHECK /
@@ -391,8 +412,8 @@ pkv_status pkv_set_wait_limit_ns(int64_t limit_ns);
  * Kernel timing: while enabled, every kernel launch of the library is
  * bracketed by CUDA events on its own stream.  pkv_profiler_read
  * synchronises the recorded events and returns, for kernel `name`
- * ("store_kvcache", "decode", "prefill", "store_kvcache_int8",
- * "decode_int8"), the summed
+ * ("store_kvcache", "decode", "decode_append", "shared_prefix", "prefill",
+ * "store_kvcache_int8", "decode_int8", "prefill_int8"), the summed
  * duration in milliseconds and the launch count since the last reset.
  */
 pkv_status pkv_profiler_enable(int32_t enable);

@@ -47,6 +47,8 @@ SIGNATURES = {
                                 _P], _I32),
     "pkv_decode_attention_int8": ([_P, _I64, _P, _P, _P, _P, _I64, _P, _I32, _P, _I32, _I32,
                                    _I32, _I32, _F, _P, _P], _I32),
+    "pkv_prefill_attention_int8": ([_P, _I64, _P, _P, _P, _P, _I64, _P, _I32, _P, _P, _I32, _I64,
+                                    _I32, _I32, _I32, _F, _P, _P], _I32),
     "pkv_status_string": ([_I32], ctypes.c_char_p),
     "pkv_version": ([], ctypes.c_char_p),
     "pkv_get_device_error": ([_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)], _I32),
@@ -318,6 +320,28 @@ def pkv_decode_attention_int8(q, k_codes, v_codes, k_scales, v_scales, block_tab
         _ptr(q), qs, _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), nb,
         _ptr(block_tables), int(block_tables.shape[1]), _ptr(context_lens), b, hq, hkv, d,
         float(scale), _ptr(out), _stream(stream)), "pkv_decode_attention_int8")
+
+
+def pkv_prefill_attention_int8(q, k_codes, v_codes, k_scales, v_scales, block_tables,
+                               cu_seqlens_q, context_lens, scale: float, out, stream=None) -> None:
+    """Chunked causal prefill over the INT8 cache: q [T, Hq, D] -> out [T, Hq, D]."""
+    import torch
+    nb, hkv, d = _int8_cache(k_codes, v_codes, k_scales, v_scales)
+    _need(q.dim() == 3, "q: [T, Hq, D]")
+    t, hq = int(q.shape[0]), int(q.shape[1])
+    qs = _rows(q, "q", hq, d)
+    for x, n in ((block_tables, "block_tables"), (cu_seqlens_q, "cu_seqlens_q"),
+                 (context_lens, "context_lens")):
+        _i32(x, n)
+    b = int(context_lens.numel())
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == b, "block_tables: [B, max_blocks]")
+    _need(cu_seqlens_q.numel() == b + 1, "cu_seqlens_q: [B + 1]")
+    _need(out.is_cuda and out.dtype == torch.bfloat16 and out.is_contiguous()
+          and tuple(out.shape) == (t, hq, d), "out: contiguous bf16 CUDA [T, Hq, D]")
+    _check(load_library().pkv_prefill_attention_int8(
+        _ptr(q), qs, _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), nb,
+        _ptr(block_tables), int(block_tables.shape[1]), _ptr(cu_seqlens_q), _ptr(context_lens),
+        b, t, hq, hkv, d, float(scale), _ptr(out), _stream(stream)), "pkv_prefill_attention_int8")
 
 
 def pkv_get_device_error(stream=None):

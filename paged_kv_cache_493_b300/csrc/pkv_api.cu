@@ -170,18 +170,22 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
 }
 
 // Tensor maps over INT8 codes [num_blocks][Hkv][256][D] bytes viewed as 3-D
-// {D, 256, num_blocks * Hkv} for the decode: box {D, 32, 1} (32 consecutive
-// tokens of one (block, KV head), one contiguous tile), 128-byte swizzle for
-// D = 128 and 64-byte for D = 64 (the swizzle span is the row).
+// {D, 256, num_blocks * Hkv}; a box of `rows` consecutive tokens of one
+// (block, KV head) is one contiguous tile.  The decode takes 32 rows with the
+// 128-byte swizzle for D = 128 and 64-byte for D = 64 (the swizzle span is
+// the row); the prefill takes 64 rows unswizzled (its producers dequantise
+// them with plain loads).
 bool encode_int8_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k, const void* v,
-                      int64_t num_blocks, int hkv, int d) {
+                      int64_t num_blocks, int hkv, int d, bool prefill = false) {
   const uint64_t tiles = static_cast<uint64_t>(num_blocks) * hkv;
   const uint64_t blk = pkv::kBlockSize;
-  const CUtensorMapSwizzle swz =
-      d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  return encode_3d(kmap, k, d, blk, tiles, d, blk * d, d, pkv::kDecodeChunk, 1, swz,
+  const uint32_t rows = prefill ? pkv::kPrefillKeyTile : pkv::kDecodeChunk;
+  const CUtensorMapSwizzle swz = prefill    ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                 : d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                            : CU_TENSOR_MAP_SWIZZLE_64B;
+  return encode_3d(kmap, k, d, blk, tiles, d, blk * d, d, rows, 1, swz,
                    CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
-         encode_3d(vmap, v, d, blk, tiles, d, blk * d, d, pkv::kDecodeChunk, 1, swz,
+         encode_3d(vmap, v, d, blk, tiles, d, blk * d, d, rows, 1, swz,
                    CU_TENSOR_MAP_DATA_TYPE_UINT8);
 }
 
@@ -751,6 +755,61 @@ pkv_status pkv_prefill_attention(const void* q, int64_t q_row_stride, const void
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return cuda_status(
       timed_launch("prefill", s, [&] { return pkv::launch_prefill(a, m, qmap, num_sms, s); }));
+}
+
+pkv_status pkv_prefill_attention_int8(const void* q, int64_t q_row_stride, const int8_t* k_codes,
+                                      const int8_t* v_codes, const float* k_scales,
+                                      const float* v_scales, int64_t num_blocks,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                                      int32_t num_seqs, int64_t total_q, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, float scale,
+                                      void* out, pkv_stream_t stream) {
+  pkv_status st = pkv::validate_attention_args(q, q_row_stride, k_codes, v_codes, num_blocks,
+                                               block_tables, max_blocks_per_seq, context_lens,
+                                               num_seqs, num_q_heads, num_kv_heads, head_dim, out);
+  if (st != PKV_OK) return st;
+  if (!cu_seqlens_q || total_q < 0 || total_q > 0x7FFFFFFF) return PKV_ERR_INVALID_ARG;
+  if (!k_scales || !v_scales) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_scales) || !aligned16(v_scales)) return PKV_ERR_UNSUPPORTED;
+  pkv::PrefillArgs a{};
+  CUtensorMap kmap, vmap, qmap;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = device_state(&st);
+    if (!ds) return st;
+    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    if (!encode_int8_maps(&kmap, &vmap, k_codes, v_codes, num_blocks, num_kv_heads, head_dim,
+                          true))
+      return PKV_ERR_CUDA;
+    const int g = num_q_heads / num_kv_heads;
+    if (!encode_3d(&qmap, q, head_dim, num_q_heads, total_q, static_cast<uint64_t>(head_dim) * 2,
+                   static_cast<uint64_t>(q_row_stride) * 2, 64, g, 128 / g,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return PKV_ERR_CUDA;
+    a.q = q;
+    a.q_row_stride = q_row_stride;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.wait_limit_ns = static_cast<uint64_t>(g_wait_limit_ns.load());
+    a.err = ds->err;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed_launch("prefill_int8", s, [&] {
+    return pkv::launch_prefill_i8(a, kmap, vmap, qmap, s);
+  }));
 }
 
 pkv_status pkv_get_device_error(pkv_stream_t stream, int32_t* code, int32_t* info) {

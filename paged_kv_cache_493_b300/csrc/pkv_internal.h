@@ -89,7 +89,9 @@ struct DecodeArgs {
   const float* v_scales;
 };
 
-// Most units (key ranges) the shared prefix of a cascade decode is cut into.
+// Most partial states per row the decode's fold of a shared prefix accepts
+// (DecodeArgs::shared_units; the cascade's shared-prefix kernel merges its
+// units in the cluster and leaves one).
 constexpr int kMaxSharedUnits = 32;
 
 struct PrefillArgs {
@@ -112,19 +114,24 @@ struct PrefillArgs {
   // Shared-prefix role of the cascade decode (launch_shared_prefix only):
   // the decode queries of all num_seqs sequences attend the first
   // shared_tiles * 64 tokens reached through table row 0, cut into
-  // shared_units key ranges; row (s * G + g) of KV head h, unit u, leaves its
-  // partial state at index (h * shared_units + u) * shared_rows_pad + row of
-  // shared_o ([..][head_dim] fp32, unnormalised) and shared_ml ([..][2]: the
+  // shared_units key ranges, one CTA each; the units of a (row tile, KV head)
+  // form a cluster and merge their states, and row (s * G + g) of KV head h
+  // leaves the merged state at index h * shared_rows_pad + row of shared_o
+  // ([..][head_dim] fp32, unnormalised) and shared_ml ([..][2]: the
   // reference max in the log2 domain and the sum; sum -1 marks a failed row).
   int shared_tiles;
   int shared_units;
   int shared_rows_pad;  // row tiles * 128
   float* shared_o;
   float* shared_ml;
+  // INT8 cache (launch_prefill_i8 only): scales [num_blocks][Hkv][256].
+  const float* k_scales;
+  const float* v_scales;
 };
 
-// INT8 KV cache: codes int8 [num_blocks][256][Hkv][D], scales float32
-// [num_blocks][256][Hkv]; a code stands for code * scale.
+// INT8 KV cache: codes int8 [num_blocks][Hkv][256][D], scales float32
+// [num_blocks][Hkv][256] (each block holds its KV heads one after another);
+// a code stands for code * scale.
 struct StoreI8Args {
   const void* k;
   const void* v;
@@ -168,13 +175,19 @@ size_t decode_counter_bytes(int64_t num_pairs);
 size_t decode_partial_bytes(int num_ctas, int group, int head_dim);
 cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream);
 // The same split-K decode over an INT8 cache: kmap / vmap view the codes as
-// uint8 {D, Hkv, slots} with box {D, 1, 32} (128-byte swizzle for D = 128,
-// 64-byte for D = 64); a.k_scales / a.v_scales are set.  At most 8 KV heads.
+// uint8 {D, 256, num_blocks * Hkv} with box {D, 32, 1} (128-byte swizzle for
+// D = 128, 64-byte for D = 64); a.k_scales / a.v_scales are set.
 cudaError_t launch_decode_i8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream);
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream);
+// The same prefill over an INT8 cache: kmap / vmap view the codes as uint8
+// {D, 256, num_blocks * Hkv} with box {D, 64, 1}, no swizzle; a.k_scales /
+// a.v_scales are set.
+cudaError_t launch_prefill_i8(const PrefillArgs& a, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const CUtensorMap& qmap,
+                              cudaStream_t stream);
 // The shared-prefix kernel of the cascade decode (qmap: the decode queries
 // viewed as {D, Hq, num_seqs} with the prefill's box).
 cudaError_t launch_shared_prefix(const PrefillArgs& a, const CacheMaps& maps,

@@ -71,6 +71,11 @@ struct PrefillLayout {
   static constexpr int kMergeW = kRowMl + kRows * 8;     // float [128] (rows x units)
   static constexpr int kMergeRow = kMergeW + kRows * 4;  // float M, L; int bad [<= 128]
   static constexpr int kBytes = kMergeRow + kRows * 12;
+  // INT8 cache only (the shared-prefix region is unused there): the scales
+  // of the K and V tiles in flight, float [2 stages][64] each.
+  static constexpr int kKScales = kRowMl;
+  static constexpr int kVScales = kKScales + kKvStages * kKeyTile * 4;
+  static_assert(kVScales + kKvStages * kKeyTile * 4 <= kBytes, "scale stages fit");
   // After the last PV the Q/K/V buffers are free: each row's O (fp32) is
   // staged there for the cluster merge, rows padded by 4 floats.
   static constexpr int kOStride = D + 4;
@@ -81,15 +86,19 @@ struct PrefillBars {
   uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
       pv_done[2], drain;
 };
+// Byte offsets, from the first barrier, of stage 0's barriers (stage 1: + 8).
+constexpr uint32_t kBarKFull = 8, kBarKEmpty = 24, kBarVFull = 40, kBarVEmpty = 56;
+// INT8 cache only: the codes and scales of a K (V) stage have landed.
+constexpr uint32_t kBarKRaw = 128, kBarVRaw = 144;
 
 __device__ __forceinline__ PrefillBars make_bars(uint32_t base) {
   PrefillBars b;
   b.q_full = base;
   for (int s = 0; s < 2; ++s) {
-    b.k_full[s] = base + 8 + 8 * s;
-    b.k_empty[s] = base + 24 + 8 * s;
-    b.v_full[s] = base + 40 + 8 * s;
-    b.v_empty[s] = base + 56 + 8 * s;
+    b.k_full[s] = base + kBarKFull + 8 * s;
+    b.k_empty[s] = base + kBarKEmpty + 8 * s;
+    b.v_full[s] = base + kBarVFull + 8 * s;
+    b.v_empty[s] = base + kBarVEmpty + 8 * s;
     b.s_full[s] = base + 72 + 8 * s;
     b.p_full[s] = base + 88 + 8 * s;
     b.pv_done[s] = base + 104 + 8 * s;
@@ -129,6 +138,75 @@ __device__ __forceinline__ TileInfo find_tile(const PrefillArgs& a, int t, int q
   return ti;
 }
 
+// Four int8 codes (one word) times their row's scale, as two bf16 pairs
+// (round to nearest even).  A code c becomes exact in fp32 as the float with
+// bit pattern 0x4B0000xx, xx = c + 128 (that is 2^23 + c + 128), minus
+// 2^23 + 128; the product with the scale is rounded to fp32, then to bf16.
+__device__ __forceinline__ void dequant4(uint32_t w, uint64_t s2, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint64_t bias = f2_pack(-8388736.0f, -8388736.0f);
+  const uint64_t c01 = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                      __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))),
+                              bias);
+  const uint64_t c23 = f2_add(f2_pack(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                      __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))),
+                              bias);
+  float x0, x1, x2, x3;
+  f2_unpack(f2_mul(c01, s2), x0, x1);
+  f2_unpack(f2_mul(c23, s2), x2, x3);
+  lo = pack_bf16x2(x0, x1);
+  hi = pack_bf16x2(x2, x3);
+}
+
+// One warp turns a stage holding an INT8 tile -- 64 keys x D codes, key k at
+// byte k * D (no swizzle), and the keys' scales -- into the bf16 tile the
+// tensor cores read, in place: 64-column panels of 128-byte rows with the
+// 128-byte swizzle.  D / 16 lanes share a key, 16 codes each.  A key's bf16
+// row overlaps only the codes of keys >= its own (for D = 128 exactly its
+// own; for D = 64 those of keys 2k and 2k + 1), so batches are taken from
+// the last key down, and a batch reads all its codes before any lane
+// writes.
+template <int D>
+__device__ __forceinline__ void dequant_stage(uint8_t* stage, const float* scales, int lane) {
+  constexpr int kLanesPerKey = D / 16;
+  constexpr int kKeysPerPass = 32 / kLanesPerKey;
+  constexpr int kPasses = 4;
+  constexpr int kKeysPerBatch = kKeysPerPass * kPasses;
+  constexpr int kPanelBytes = kKeyTile * 128;
+  const int piece = lane % kLanesPerKey;  // codes 16 piece .. 16 piece + 15
+  const int kk = lane / kLanesPerKey;
+  const int panel = piece >> 2;
+  const int ch0 = (2 * piece) & 7;
+  // Panel-1 lanes store their odd chunk first: the eight lanes of a store
+  // phase then hit eight different 16-byte bank groups.
+  const int first = ch0 + (panel & 1), second = ch0 + 1 - (panel & 1);
+#pragma unroll 1
+  for (int b = kKeyTile / kKeysPerBatch - 1; b >= 0; --b) {
+    uint4 c[kPasses];
+    float sc[kPasses];
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p) {
+      const int k = b * kKeysPerBatch + p * kKeysPerPass + kk;
+      c[p] = *reinterpret_cast<const uint4*>(stage + k * D + piece * 16);
+      sc[p] = scales[k];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int p = 0; p < kPasses; ++p) {
+      const int k = b * kKeysPerBatch + p * kKeysPerPass + kk;
+      const uint64_t s2 = f2_pack(sc[p], sc[p]);
+      uint4 lo, hi;  // codes 0-7 and 8-15 of the piece
+      dequant4(c[p].x, s2, lo.x, lo.y);
+      dequant4(c[p].y, s2, lo.z, lo.w);
+      dequant4(c[p].z, s2, hi.x, hi.y);
+      dequant4(c[p].w, s2, hi.z, hi.w);
+      uint8_t* row = stage + panel * kPanelBytes;
+      *reinterpret_cast<uint4*>(row + sw128_offset(k, first)) = first == ch0 ? lo : hi;
+      *reinterpret_cast<uint4*>(row + sw128_offset(k, second)) = second == ch0 ? lo : hi;
+    }
+  }
+}
+
 // kShared = false: chunked causal prefill (grid: tiles x KV heads).
 // kShared = true: the shared-prefix role of the cascade decode (grid: row
 // tiles x units x KV heads).  The "queries" of a tile are then 128/G
@@ -138,10 +216,16 @@ __device__ __forceinline__ TileInfo find_tile(const PrefillArgs& a, int t, int q
 // epilogue writes each row's partial state -- the reference max m (log2
 // domain), the sum l and the unnormalised O, fp32 -- for the decode kernel
 // to merge with the sequence's private part.
-template <int D, int G, bool kShared>
+// kI8 = true (with kShared = false): the cache holds INT8 codes and scales
+// (head-major blocks); kmap / vmap view the codes as {D, 256, blocks x Hkv}
+// with box {D, 64, 1}.  The two producer warps load a stage's codes and
+// scales and, all 32 lanes, dequantise it in place to the bf16 layout of the
+// bf16 cache; the MMA and softmax warps are unchanged.
+template <int D, int G, bool kShared, bool kI8>
 __global__ void __launch_bounds__(kPrefillThreads, kCtasPerSm)
 prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, PrefillArgs a) {
+  static_assert(!(kShared && kI8), "no INT8 shared-prefix role");
   using L = PrefillLayout<D>;
   constexpr int QT = kRows / G;  // queries per tile
   constexpr uint32_t kKTileBytes = kKeyTile * D * 2;
@@ -183,6 +267,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(bar.pv_done[s], 1);
     }
     mbar_init(bar.drain, 1);
+    if constexpr (kI8) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(sbase + L::kBar + kBarKRaw + 8 * s, 1);
+        mbar_init(sbase + L::kBar + kBarVRaw + 8 * s, 1);
+      }
+    }
     misc[1] = 0;
     misc[2] = 0;
     fence_barrier_init();
@@ -248,7 +338,97 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     report_error(a.err, kErrDeviceCheck, bad ? kSitePrefillChunk : kSitePrefillBlock);
   const bool run = ti.valid && !bad && misc[2] == 0 && nkt > 0;
 
-  if (warp == kProducerWarp) {
+  if (kI8 && (warp == kProducerWarp || warp == kVProducerWarp)) {
+    // ------------------------------------------------- INT8 producers (Q, K) and (V)
+    // Event loop of the whole warp (lane 0 decides, the warp follows):
+    // issue the next tile's codes and scales into a free stage, or
+    // dequantise the oldest stage that has landed and hand it to the MMA.
+    if (run) {
+      const bool is_k = warp == kProducerWarp;
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      const float* gscales = is_k ? a.k_scales : a.v_scales;
+      // Stage st's barriers: raw + 8 st (copies landed), full + 8 st (bf16
+      // tile ready for the MMA), empty + 8 st (the MMA is done with it).
+      const uint32_t bars = sbase + L::kBar;
+      const uint32_t raw = bars + (is_k ? kBarKRaw : kBarVRaw);
+      const uint32_t full = bars + (is_k ? kBarKFull : kBarVFull);
+      const uint32_t empty = bars + (is_k ? kBarKEmpty : kBarVEmpty);
+      const int stage0 = is_k ? L::kK : L::kV;
+      const int scale0 = is_k ? L::kKScales : L::kVScales;
+      const int site = kSitePrefillWait + (is_k ? 8 : 9);
+      constexpr uint32_t kCodeBytes = kKeyTile * D;
+      constexpr uint32_t kScaleBytes = kKeyTile * 4;
+      constexpr int kStageBytes = L::kPanels * L::kKvPanel;
+      if (is_k && lane == 0) {
+        mbar_arrive_expect_tx(bar.q_full, kQBytes);
+#pragma unroll
+        for (int p = 0; p < L::kPanels; ++p)
+          tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full, p * 64, kvh * G,
+                      ti.q_row0 + ti.qt_start);
+      }
+      int ji = 0, jc = 0;  // next tile to issue, to convert
+      bool idle = false;
+      uint64_t idle_since = 0;
+      while (jc < nkt) {
+        int act = 0;  // 1 issue, 2 convert, -1 stop
+        if (lane == 0) {
+          if (misc[1]) {
+            act = -1;
+          } else if (ji < nkt &&
+                     (ji < kKvStages || mbar_test(empty + 8 * (ji & 1), ((ji >> 1) - 1) & 1))) {
+            act = 1;
+          } else if (jc < ji && mbar_test(raw + 8 * (jc & 1), (jc >> 1) & 1)) {
+            act = 2;
+          } else {
+            const uint64_t now = global_timer_ns();
+            if (!idle) {
+              idle = true;
+              idle_since = now;
+            } else if (now - idle_since > a.wait_limit_ns) {
+              report_error(a.err, kErrTimeout, site);
+              misc[1] = 1;
+              act = -1;
+            }
+          }
+          if (act != 0) idle = false;
+        }
+        act = __shfl_sync(0xffffffffu, act, 0);
+        if (act < 0) break;
+        if (act == 1) {
+          if (lane == 0) {
+            const int st = ji & 1;
+            const int k0 = kbase + ji * kKeyTile;
+            const int row = k0 % kBlockSize;
+            const int tile_id = table[k0 / kBlockSize] * a.num_kv_heads + kvh;
+            const uint32_t rb = raw + 8 * st;
+            mbar_arrive_expect_tx(rb, kCodeBytes + kScaleBytes);
+            tma_load_3d(sbase + stage0 + st * kStageBytes, map, rb, 0, row, tile_id);
+            bulk_load(sbase + scale0 + st * static_cast<int>(kScaleBytes),
+                      gscales + static_cast<int64_t>(tile_id) * kBlockSize + row, kScaleBytes, rb);
+          }
+          ++ji;
+        } else if (act == 2) {
+          const int st = jc & 1;
+          // Completed phase: returns at once, and makes the copied bytes
+          // visible to every lane.
+          mbar_wait(raw + 8 * st, (jc >> 1) & 1, kDrainLimitNs);
+          dequant_stage<D>(sgen + stage0 + st * kStageBytes,
+                           reinterpret_cast<const float*>(sgen + scale0) + st * kKeyTile, lane);
+          fence_proxy_async_smem();  // the tensor cores read what the lanes wrote
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full + 8 * st);
+          ++jc;
+        } else {
+          __nanosleep(64);
+        }
+      }
+      if (lane == 0) {
+        // Every copy issued must land before the block may exit.
+        if (is_k) mbar_wait(bar.q_full, 0, kDrainLimitNs);
+        for (int t = jc; t < ji; ++t) mbar_wait(raw + 8 * (t & 1), (t >> 1) & 1, kDrainLimitNs);
+      }
+    }
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (Q, K)
     if (lane == 0 && run) {
       int k_last[2] = {-1, -1};
@@ -646,11 +826,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
-template <int D, int G, bool kShared>
-cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
-                     cudaStream_t stream) {
+template <int D, int G, bool kShared, bool kI8>
+cudaError_t launch_t(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     const CUtensorMap& qmap, cudaStream_t stream) {
   using L = PrefillLayout<D>;
-  auto kern = prefill_kernel<D, G, kShared>;
+  auto kern = prefill_kernel<D, G, kShared, kI8>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
@@ -694,18 +874,18 @@ cudaError_t launch_t(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
   cfg.dynamicSmemBytes = L::kBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
-  return cudaLaunchKernelEx(&cfg, kern, qmap, maps.k_sw128, maps.v_sw128, a);
+  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, a);
 }
 
-template <int D, bool kShared>
-cudaError_t launch_d(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
-                     cudaStream_t stream) {
+template <int D, bool kShared, bool kI8>
+cudaError_t launch_d(const PrefillArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     const CUtensorMap& qmap, cudaStream_t stream) {
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_t<D, 1, kShared>(a, maps, qmap, stream);
-    case 2: return launch_t<D, 2, kShared>(a, maps, qmap, stream);
-    case 4: return launch_t<D, 4, kShared>(a, maps, qmap, stream);
-    case 8: return launch_t<D, 8, kShared>(a, maps, qmap, stream);
-    case 16: return launch_t<D, 16, kShared>(a, maps, qmap, stream);
+    case 1: return launch_t<D, 1, kShared, kI8>(a, kmap, vmap, qmap, stream);
+    case 2: return launch_t<D, 2, kShared, kI8>(a, kmap, vmap, qmap, stream);
+    case 4: return launch_t<D, 4, kShared, kI8>(a, kmap, vmap, qmap, stream);
+    case 8: return launch_t<D, 8, kShared, kI8>(a, kmap, vmap, qmap, stream);
+    case 16: return launch_t<D, 16, kShared, kI8>(a, kmap, vmap, qmap, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -715,8 +895,17 @@ cudaError_t launch_d(const PrefillArgs& a, const CacheMaps& maps, const CUtensor
 cudaError_t launch_prefill(const PrefillArgs& a, const CacheMaps& maps, const CUtensorMap& qmap,
                            int num_sms, cudaStream_t stream) {
   (void)num_sms;
-  if (a.head_dim == 128) return launch_d<128, false>(a, maps, qmap, stream);
-  if (a.head_dim == 64) return launch_d<64, false>(a, maps, qmap, stream);
+  if (a.head_dim == 128) return launch_d<128, false, false>(a, maps.k_sw128, maps.v_sw128, qmap, stream);
+  if (a.head_dim == 64) return launch_d<64, false, false>(a, maps.k_sw128, maps.v_sw128, qmap, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_i8(const PrefillArgs& a, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const CUtensorMap& qmap,
+                              cudaStream_t stream) {
+  if (!a.k_scales || !a.v_scales) return cudaErrorInvalidValue;
+  if (a.head_dim == 128) return launch_d<128, false, true>(a, kmap, vmap, qmap, stream);
+  if (a.head_dim == 64) return launch_d<64, false, true>(a, kmap, vmap, qmap, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -725,8 +914,8 @@ cudaError_t launch_shared_prefix(const PrefillArgs& a, const CacheMaps& maps,
   if (a.shared_units <= 0 || a.shared_units > 16 || (a.shared_units & (a.shared_units - 1)) ||
       a.shared_tiles < a.shared_units)
     return cudaErrorInvalidValue;
-  if (a.head_dim == 128) return launch_d<128, true>(a, maps, qmap, stream);
-  if (a.head_dim == 64) return launch_d<64, true>(a, maps, qmap, stream);
+  if (a.head_dim == 128) return launch_d<128, true, false>(a, maps.k_sw128, maps.v_sw128, qmap, stream);
+  if (a.head_dim == 64) return launch_d<64, true, false>(a, maps.k_sw128, maps.v_sw128, qmap, stream);
   return cudaErrorInvalidValue;
 }
 
