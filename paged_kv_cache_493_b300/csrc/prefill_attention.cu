@@ -82,30 +82,28 @@ struct PrefillLayout {
   static_assert(kRows * kOStride * 4 <= kBar, "O staging fits in the Q/K/V buffers");
 };
 
-struct PrefillBars {
-  uint32_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
-      pv_done[2], drain;
-};
-// Byte offsets, from the first barrier, of stage 0's barriers (stage 1: + 8).
+// Barrier addresses from the first barrier's: computed, not stored, so a
+// stage picked at run time costs no local-memory load on the hot loops.
+// Byte offsets of stage 0's barriers (stage 1: + 8).
 constexpr uint32_t kBarKFull = 8, kBarKEmpty = 24, kBarVFull = 40, kBarVEmpty = 56;
+constexpr uint32_t kBarSFull = 72, kBarPFull = 88, kBarPvDone = 104, kBarDrain = 120;
 // INT8 cache only: the codes and scales of a K (V) stage have landed.
 constexpr uint32_t kBarKRaw = 128, kBarVRaw = 144;
 
-__device__ __forceinline__ PrefillBars make_bars(uint32_t base) {
-  PrefillBars b;
-  b.q_full = base;
-  for (int s = 0; s < 2; ++s) {
-    b.k_full[s] = base + kBarKFull + 8 * s;
-    b.k_empty[s] = base + kBarKEmpty + 8 * s;
-    b.v_full[s] = base + kBarVFull + 8 * s;
-    b.v_empty[s] = base + kBarVEmpty + 8 * s;
-    b.s_full[s] = base + 72 + 8 * s;
-    b.p_full[s] = base + 88 + 8 * s;
-    b.pv_done[s] = base + 104 + 8 * s;
-  }
-  b.drain = base + 120;
-  return b;
-}
+struct PrefillBars {
+  uint32_t base;
+  __device__ __forceinline__ uint32_t q_full() const { return base; }
+  __device__ __forceinline__ uint32_t k_full(int s) const { return base + kBarKFull + 8 * s; }
+  __device__ __forceinline__ uint32_t k_empty(int s) const { return base + kBarKEmpty + 8 * s; }
+  __device__ __forceinline__ uint32_t v_full(int s) const { return base + kBarVFull + 8 * s; }
+  __device__ __forceinline__ uint32_t v_empty(int s) const { return base + kBarVEmpty + 8 * s; }
+  __device__ __forceinline__ uint32_t s_full(int s) const { return base + kBarSFull + 8 * s; }
+  __device__ __forceinline__ uint32_t p_full(int s) const { return base + kBarPFull + 8 * s; }
+  __device__ __forceinline__ uint32_t pv_done(int s) const { return base + kBarPvDone + 8 * s; }
+  __device__ __forceinline__ uint32_t drain() const { return base + kBarDrain; }
+};
+
+__device__ __forceinline__ PrefillBars make_bars(uint32_t base) { return PrefillBars{base}; }
 
 struct TileInfo {
   int seq, qt_start, lq, ctx, q_row0;
@@ -256,17 +254,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   const int unit = kShared ? blockIdx.x % a.shared_units : 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar.q_full, 1);
+    mbar_init(bar.q_full(), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar.k_full[s], 1);
-      mbar_init(bar.k_empty[s], 1);
-      mbar_init(bar.v_full[s], 1);
-      mbar_init(bar.v_empty[s], 1);
-      mbar_init(bar.s_full[s], 1);
-      mbar_init(bar.p_full[s], kSoftmaxWarps * 32);
-      mbar_init(bar.pv_done[s], 1);
+      mbar_init(bar.k_full(s), 1);
+      mbar_init(bar.k_empty(s), 1);
+      mbar_init(bar.v_full(s), 1);
+      mbar_init(bar.v_empty(s), 1);
+      mbar_init(bar.s_full(s), 1);
+      mbar_init(bar.p_full(s), kSoftmaxWarps * 32);
+      mbar_init(bar.pv_done(s), 1);
     }
-    mbar_init(bar.drain, 1);
+    mbar_init(bar.drain(), 1);
     if constexpr (kI8) {
       for (int s = 0; s < 2; ++s) {
         mbar_init(sbase + L::kBar + kBarKRaw + 8 * s, 1);
@@ -360,10 +358,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       constexpr uint32_t kScaleBytes = kKeyTile * 4;
       constexpr int kStageBytes = L::kPanels * L::kKvPanel;
       if (is_k && lane == 0) {
-        mbar_arrive_expect_tx(bar.q_full, kQBytes);
+        mbar_arrive_expect_tx(bar.q_full(), kQBytes);
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full, p * 64, kvh * G,
+          tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full(), p * 64, kvh * G,
                       ti.q_row0 + ti.qt_start);
       }
       int ji = 0, jc = 0;  // next tile to issue, to convert
@@ -424,7 +422,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
       if (lane == 0) {
         // Every copy issued must land before the block may exit.
-        if (is_k) mbar_wait(bar.q_full, 0, kDrainLimitNs);
+        if (is_k) mbar_wait(bar.q_full(), 0, kDrainLimitNs);
         for (int t = jc; t < ji; ++t) mbar_wait(raw + 8 * (t & 1), (t >> 1) & 1, kDrainLimitNs);
       }
     }
@@ -432,35 +430,35 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // ------------------------------------------------------------ producer (Q, K)
     if (lane == 0 && run) {
       int k_last[2] = {-1, -1};
-      mbar_arrive_expect_tx(bar.q_full, kQBytes);
+      mbar_arrive_expect_tx(bar.q_full(), kQBytes);
 #pragma unroll
       for (int p = 0; p < L::kPanels; ++p)
-        tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full, p * 64, kvh * G,
+        tma_load_3d(sbase + L::kQ + p * L::kQPanel, &qmap, bar.q_full(), p * 64, kvh * G,
                     ti.q_row0 + ti.qt_start);
       for (int j = 0; j < nkt; ++j) {
         const int st = j & 1;
         const int k0 = kbase + j * kKeyTile;
         const int slot = table[k0 / kBlockSize] * kBlockSize + (k0 % kBlockSize);
         if (j >= kKvStages &&
-            !mbar_wait(bar.k_empty[st], ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
+            !mbar_wait(bar.k_empty(st), ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
           report_error(a.err, kErrTimeout, kSitePrefillWait + 0);
           misc[1] = 1;
           break;
         }
         if (misc[1]) break;
-        mbar_arrive_expect_tx(bar.k_full[st], kKTileBytes);
+        mbar_arrive_expect_tx(bar.k_full(st), kKTileBytes);
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sbase + L::kK + (st * L::kPanels + p) * L::kKvPanel, &kmap, bar.k_full[st],
+          tma_load_3d(sbase + L::kK + (st * L::kPanels + p) * L::kKvPanel, &kmap, bar.k_full(st),
                       p * 64, kvh, slot);
         k_last[st] = j;
       }
       // Every copy issued must land before the block may exit, whether or
       // not its consumer gave up on it (after a normal run these waits
       // return at once).
-      mbar_wait(bar.q_full, 0, kDrainLimitNs);
+      mbar_wait(bar.q_full(), 0, kDrainLimitNs);
       for (int s = 0; s < 2; ++s)
-        if (k_last[s] >= 0) mbar_wait(bar.k_full[s], (k_last[s] >> 1) & 1, kDrainLimitNs);
+        if (k_last[s] >= 0) mbar_wait(bar.k_full(s), (k_last[s] >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kVProducerWarp) {
     // ------------------------------------------------------------ producer (V)
@@ -471,28 +469,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const int k0 = kbase + j * kKeyTile;
         const int slot = table[k0 / kBlockSize] * kBlockSize + (k0 % kBlockSize);
         if (j >= kKvStages &&
-            !mbar_wait(bar.v_empty[st], ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
+            !mbar_wait(bar.v_empty(st), ((j >> 1) - 1) & 1, a.wait_limit_ns)) {
           report_error(a.err, kErrTimeout, kSitePrefillWait + 1);
           misc[1] = 1;
           break;
         }
         if (misc[1]) break;
-        mbar_arrive_expect_tx(bar.v_full[st], kKTileBytes);
+        mbar_arrive_expect_tx(bar.v_full(st), kKTileBytes);
 #pragma unroll
         for (int p = 0; p < L::kPanels; ++p)
-          tma_load_3d(sbase + L::kV + (st * L::kPanels + p) * L::kKvPanel, &vmap, bar.v_full[st],
+          tma_load_3d(sbase + L::kV + (st * L::kPanels + p) * L::kKvPanel, &vmap, bar.v_full(st),
                       p * 64, kvh, slot);
         v_last[st] = j;
       }
       for (int s = 0; s < 2; ++s)
-        if (v_last[s] >= 0) mbar_wait(bar.v_full[s], (v_last[s] >> 1) & 1, kDrainLimitNs);
+        if (v_last[s] >= 0) mbar_wait(bar.v_full(s), (v_last[s] >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && run) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeyTile, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, true);
-      bool ok = mbar_wait(bar.q_full, 0, a.wait_limit_ns);
+      bool ok = mbar_wait(bar.q_full(), 0, a.wait_limit_ns);
       if (!ok) report_error(a.err, kErrTimeout, kSitePrefillWait + 2);
       int js = 0, jp = 0;
       bool idle = false;
@@ -501,7 +499,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         bool did = false;
         // S_js overwrites the columns where P_{js-2} sits: only after PV_{js-2}
         // has been issued (the tensor pipe executes in order).
-        if (js < nkt && js - 2 < jp && mbar_test(bar.k_full[js & 1], (js >> 1) & 1)) {  // S_js = Q K_js^T
+        if (js < nkt && js - 2 < jp && mbar_test(bar.k_full(js & 1), (js >> 1) & 1)) {  // S_js = Q K_js^T
           const int st = js & 1;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kSCol0 + st * kKeyTile;
@@ -514,13 +512,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 smem_desc_sw128(sbase + L::kK + st * L::kPanels * L::kKvPanel + koff, 16, 1024);
             tc_mma_ss(d_tmem, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
           }
-          tc_commit(bar.s_full[st]);
-          tc_commit(bar.k_empty[st]);
+          tc_commit(bar.s_full(st));
+          tc_commit(bar.k_empty(st));
           ++js;
           did = true;
         }
-        if (jp < js && mbar_test(bar.p_full[jp & 1], (jp >> 1) & 1) &&
-            mbar_test(bar.v_full[jp & 1], (jp >> 1) & 1)) {  // O += P_jp V_jp
+        if (jp < js && mbar_test(bar.p_full(jp & 1), (jp >> 1) & 1) &&
+            mbar_test(bar.v_full(jp & 1), (jp >> 1) & 1)) {  // O += P_jp V_jp
           const int st = jp & 1;
           tc_fence_after();
 #pragma unroll
@@ -532,8 +530,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                 sbase + L::kV + st * L::kPanels * L::kKvPanel + kk * 16 * 128, L::kKvPanel, 1024);
             tc_mma_ts(tmem + kOCol, a_tmem, bd, idesc_o, (jp > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar.pv_done[st]);
-          tc_commit(bar.v_empty[st]);
+          tc_commit(bar.pv_done(st));
+          tc_commit(bar.v_empty(st));
           ++jp;
           did = true;
         }
@@ -558,8 +556,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
       if (!ok) misc[1] = 1;
       // Every MMA issued must finish before tensor memory is released.
-      tc_commit(bar.drain);
-      mbar_wait(bar.drain, 0, kDrainLimitNs);
+      tc_commit(bar.drain());
+      mbar_wait(bar.drain(), 0, kDrainLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -578,13 +576,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const float masked = sl2 >= 0.f ? -INFINITY : INFINITY;
     for (int j = 0; ok && j < nkt; ++j) {
       // Exit decisions are warp-uniform: tcgen05.ld/st are warp-collective.
-      const bool got = mbar_wait(bar.s_full[j & 1], (j >> 1) & 1, a.wait_limit_ns);
+      const bool got = mbar_wait(bar.s_full(j & 1), (j >> 1) & 1, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 5);
-        ok = false;
-        break;
-      }
-      if (__shfl_sync(0xffffffffu, misc[1], 0)) {
         ok = false;
         break;
       }
@@ -594,7 +588,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       for (int c = 0; c < kKeyTile / 32; ++c)
         tmem_ld_32x32b_x32(trow + kSCol0 + (j & 1) * kKeyTile + c * 32,
                            *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+      // The abort flag is read while the loads are in flight.
+      const int abort = __shfl_sync(0xffffffffu, misc[1], 0);
       tmem_wait_ld();
+      if (abort) {
+        ok = false;
+        break;
+      }
       const int k0 = j * kKeyTile;  // key of x[0]
       if (!kShared && ((k0 + kKeyTile - 1 > pos_min) || (k0 + kKeyTile > ti.ctx))) {
 #pragma unroll
@@ -626,7 +626,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (j >= 1) {
           // O holds PV up to tile j - 1: wait for it before rescaling.
           const bool got_o =
-              mbar_wait(bar.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.wait_limit_ns);
+              mbar_wait(bar.pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, a.wait_limit_ns);
           if (!__all_sync(0xffffffffu, got_o)) {
             if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 6);
             ok = false;
@@ -676,12 +676,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       for (int i = 0; i < 4; ++i) f2_unpack(rs2[i], rs[i], rs[i + 4]);
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tc_fence_before();
-      mbar_arrive(bar.p_full[j & 1]);
+      mbar_arrive(bar.p_full(j & 1));
     }
     // ---- epilogue: O / l -> bf16
     if (ok && nkt > 0) {  // ok is warp-uniform here
       const bool got =
-          mbar_wait(bar.pv_done[(nkt - 1) & 1], ((nkt - 1) >> 1) & 1, a.wait_limit_ns);
+          mbar_wait(bar.pv_done((nkt - 1) & 1), ((nkt - 1) >> 1) & 1, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) report_error(a.err, kErrTimeout, kSitePrefillWait + 7);
         ok = false;
