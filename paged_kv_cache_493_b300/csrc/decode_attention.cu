@@ -636,13 +636,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         sm.slice_slot[i] = __ldg(a.slot_mapping + tab_seq0 + i);
     __syncwarp();
     if (lane == 0) {
-      // Last post of each stage (copies or descriptor only): phases of one
-      // barrier complete in order, so once that one is complete every copy
-      // ever issued into the stage has landed.
-      int last_posted[kStages];
-#pragma unroll
-      for (int s = 0; s < kStages; ++s) last_posted[s] = -1;
-      int c = 0;  // stages posted so far (stage c % kStages, phase c / kStages)
+      // Posts go to the stages in turn (post c to stage c % kStages, phase
+      // c / kStages); a claimed stage is always posted.
+      int c = 0;  // stages posted so far
       bool aborted = false;
       // Claims the next ring stage; false when the wait for it expired.
       auto claim = [&](int st) -> bool {
@@ -708,7 +704,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             }
           }
           const uint32_t fb = smem_u32(&sm.full[st]);
-          last_posted[st] = c;
           if (inf.n_valid <= 0) {
             mbar_arrive(fb);  // descriptor only
           } else {
@@ -807,16 +802,19 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const int st = c % kStages;
         if (claim(st)) {
           sm.info[st].flags = kEnd;
-          last_posted[st] = c;
           mbar_arrive(smem_u32(&sm.full[st]));
+          ++c;
         }
       }
       // Every copy issued must land before the block may exit, whether or
       // not the consumers gave up on it (after a normal run these waits
-      // return at once: the consumers have already seen each phase).
-      for (int s = 0; s < kStages; ++s)
-        if (last_posted[s] >= 0)
-          mbar_wait(smem_u32(&sm.full[s]), (last_posted[s] / kStages) & 1, kDrainLimitNs);
+      // return at once: the consumers have already seen each phase).  The
+      // last post of stage s is its newest phase: once that one is complete,
+      // every copy ever issued into the stage has landed.
+      for (int s = 0; s < kStages && s < c; ++s) {
+        const int last = s + ((c - 1 - s) / kStages) * kStages;
+        mbar_wait(smem_u32(&sm.full[s]), (last / kStages) & 1, kDrainLimitNs);
+      }
     }
   } else if (warp < kConsumerWarps) {
     // ------------------------------------------------------------ consumers

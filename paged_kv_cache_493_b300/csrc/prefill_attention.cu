@@ -429,7 +429,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer (Q, K)
     if (lane == 0 && run) {
-      int k_last[2] = {-1, -1};
+      int issued = 0;  // tiles issued (tile j into stage j & 1)
       mbar_arrive_expect_tx(bar.q_full(), kQBytes);
 #pragma unroll
       for (int p = 0; p < L::kPanels; ++p)
@@ -451,19 +451,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_3d(sbase + L::kK + (st * L::kPanels + p) * L::kKvPanel, &kmap, bar.k_full(st),
                       p * 64, kvh, slot);
-        k_last[st] = j;
+        issued = j + 1;
       }
       // Every copy issued must land before the block may exit, whether or
       // not its consumer gave up on it (after a normal run these waits
-      // return at once).
+      // return at once): the last tile issued into each stage holds its
+      // newest phase.
       mbar_wait(bar.q_full(), 0, kDrainLimitNs);
-      for (int s = 0; s < 2; ++s)
-        if (k_last[s] >= 0) mbar_wait(bar.k_full(s), (k_last[s] >> 1) & 1, kDrainLimitNs);
+      for (int t = max(issued - kKvStages, 0); t < issued; ++t)
+        mbar_wait(bar.k_full(t & 1), (t >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kVProducerWarp) {
     // ------------------------------------------------------------ producer (V)
     if (lane == 0 && run) {
-      int v_last[2] = {-1, -1};
+      int issued = 0;  // tiles issued (tile j into stage j & 1)
       for (int j = 0; j < nkt; ++j) {
         const int st = j & 1;
         const int k0 = kbase + j * kKeyTile;
@@ -480,10 +481,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int p = 0; p < L::kPanels; ++p)
           tma_load_3d(sbase + L::kV + (st * L::kPanels + p) * L::kKvPanel, &vmap, bar.v_full(st),
                       p * 64, kvh, slot);
-        v_last[st] = j;
+        issued = j + 1;
       }
-      for (int s = 0; s < 2; ++s)
-        if (v_last[s] >= 0) mbar_wait(bar.v_full(s), (v_last[s] >> 1) & 1, kDrainLimitNs);
+      for (int t = max(issued - kKvStages, 0); t < issued; ++t)
+        mbar_wait(bar.v_full(t & 1), (t >> 1) & 1, kDrainLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
