@@ -88,13 +88,14 @@ constexpr int kSliceSlots = 256;   // fused store: slots of a slice's sequences 
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
-struct StageInfo {
+struct alignas(16) StageInfo {  // 48 bytes: copied with three 16-byte accesses
   int seq, kvh, slot, n_valid, flags;
   int c_first, c_last;  // blocks holding the pair's first and last chunk
   int first_slot;       // partial slot of the pair's piece in block c_first
   // Fused store: the cache slot of the sequence's new token when this chunk
   // holds it and its row is to be stored (else -1), and its row in the chunk.
   int store_slot, store_row;
+  int pad[2];
 };
 constexpr int kFirst = 1;   // first chunk of a piece: reset the state, load q
 constexpr int kLast = 2;    // last chunk of a piece: merge and write
@@ -640,7 +641,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       // c / kStages); a claimed stage is always posted.
       int c = 0;  // stages posted so far
       bool aborted = false;
-      // Claims the next ring stage; false when the wait for it expired.
+      // Claims the next ring stage; false when the wait for it expired, or
+      // when the consumers gave up (checked every 8th post: a consumer that
+      // stopped also stops freeing stages, so a later wait expires anyway).
       auto claim = [&](int st) -> bool {
         if (c >= kStages &&
             !mbar_wait(smem_u32(&sm.empty[st]), ((c / kStages) - 1) & 1, a.wait_limit_ns)) {
@@ -648,7 +651,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           atomicExch(&sm.abort_flag, 1);
           return false;
         }
-        return *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0;
+        return (c & 7) != 0 || *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0;
       };
 
       // Emits the chunks [pos, piece_end) of one piece of sequence pseq (its
@@ -680,7 +683,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
             }
           }
-          StageInfo& inf = sm.info[st];
+          // The descriptor is built in registers and stored once.
+          StageInfo inf;
           inf.seq = pseq;
           inf.kvh = kvh;
           inf.slot = slot;
@@ -692,6 +696,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           inf.first_slot = first_slot;
           inf.store_slot = -1;
           inf.store_row = 0;
+          inf.pad[0] = inf.pad[1] = 0;
           const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
           if (fused && k == pnch - 1) {
             // The pair's last chunk holds the new token (position ctx - 1).
@@ -703,6 +708,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               report_error(a.err, kErrDeviceCheck, kSiteDecodeStoreSlot);
             }
           }
+          sm.info[st] = inf;
           const uint32_t fb = smem_u32(&sm.full[st]);
           if (inf.n_valid <= 0) {
             mbar_arrive(fb);  // descriptor only
