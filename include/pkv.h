@@ -335,7 +335,7 @@ pkv_status pkv_store_kvcache_int8(const void* k, const void* v, int64_t k_row_st
  * same result on the values the codes stand for (fp32 accumulation, bf16
  * output).  The split-K decode kernel of pkv_decode_attention (same
  * stream-K plan, in-kernel log-sum-exp merge, same workspace and the same
- * rules for CUDA graphs and overlapping calls) reading 32-token tiles of
+ * rules for CUDA graphs and overlapping calls) reading 64-token tiles of
  * codes and their scales; the codes become exact f16 values in registers,
  * the K scale multiplies each score and the V scale each probability.  Out-
  * of-range block ids or context lengths give a zero output for the sequence

@@ -74,10 +74,14 @@ namespace pkv {
 
 namespace {
 
-// Ring stages: 4 of 16 KB (K + V of a bf16 chunk at D = 128); INT8 chunks are
-// half the bytes, so 8 stages keep as many bytes in flight.
+// Tokens per chunk (the unit of the stream-K plan and of a ring stage): 32
+// for bf16, 64 for INT8, so that an INT8 stage carries as many bytes (16 KB
+// of K + V at D = 128) and the per-chunk costs (descriptor, copies, barrier
+// hand-overs) are paid per 16 KB either way.  Ring stages: 4.
 template <bool kI8>
-constexpr int kStagesOf = kI8 ? 8 : 4;
+constexpr int kChunkOf = kI8 ? 2 * kDecodeChunk : kDecodeChunk;
+template <bool kI8>
+constexpr int kStagesOf = 4;
 constexpr int kConsumerWarps = 4;  // warps 0..3: warp w computes the chunks c with c % 4 == w
 constexpr int kProducerWarp = 4;   // TMA issue
 constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
@@ -201,8 +205,8 @@ __device__ __forceinline__ const float* shared_o_at(const DecodeArgs& a, int seq
 }
 
 // The ring's K/V tiles.  bf16: per stage, D / 64 panels of 32 rows x 128
-// bytes (128-byte swizzle).  INT8: per stage, 32 rows x D bytes of codes
-// (128-byte swizzle for D = 128, 64-byte for D = 64) and the 32 tokens'
+// bytes (128-byte swizzle).  INT8: per stage, 64 rows x D bytes of codes
+// (128-byte swizzle for D = 128, 64-byte for D = 64) and the 64 tokens'
 // scales of the stage's KV head.
 template <int D, bool kI8>
 struct KvTiles {
@@ -211,10 +215,10 @@ struct KvTiles {
 };
 template <int D>
 struct KvTiles<D, true> {
-  uint8_t k[kStagesOf<true>][kDecodeChunk * D];
-  uint8_t v[kStagesOf<true>][kDecodeChunk * D];
-  alignas(16) float ks[kStagesOf<true>][kDecodeChunk];
-  alignas(16) float vs[kStagesOf<true>][kDecodeChunk];
+  uint8_t k[kStagesOf<true>][kChunkOf<true> * D];
+  uint8_t v[kStagesOf<true>][kChunkOf<true> * D];
+  alignas(16) float ks[kStagesOf<true>][kChunkOf<true>];
+  alignas(16) float vs[kStagesOf<true>][kChunkOf<true>];
 };
 
 // Byte offset of 16-byte piece `chunk` of row `row` in a TMA tile of D-byte
@@ -311,14 +315,14 @@ __device__ __forceinline__ bool bad_context(const DecodeArgs& a, int ctx, int ma
   return ctx < 0 || ctx > max_ctx || ctx < a.shared_len;
 }
 
-// Chunks of each of sequence s's pairs: ceil((C - shared_len) / 32) (the
+// Chunks of each of sequence s's pairs: ceil((C - shared_len) / kChunk) (the
 // tokens this kernel streams), and 1 for an empty private part or a rejected
 // context (that chunk carries no tokens).
+template <int kChunk>
 __device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int max_ctx) {
   const int ctx = a.context_lens[s];
   const int priv = ctx - a.shared_len;
-  return (bad_context(a, ctx, max_ctx) || priv <= 0) ? 1
-                                                      : (priv + kDecodeChunk - 1) / kDecodeChunk;
+  return (bad_context(a, ctx, max_ctx) || priv <= 0) ? 1 : (priv + kChunk - 1) / kChunk;
 }
 
 // The partial slot of the piece of a cut pair held by block cb2 (the pair
@@ -512,16 +516,18 @@ constexpr int decode_max_regs() {
   return G <= 8 ? 128 : 255;
 }
 
-// kI8 = false: bf16 cache (kmap / vmap over the bf16 pools).  kI8 = true:
-// INT8 cache (kmap / vmap over the int8 codes, box {D bytes, 1, 32}; the
-// scales a.k_scales / a.v_scales come in by plain bulk copies).
+// kI8 = false: bf16 cache (kmap / vmap over the bf16 pools), 32-token chunks.
+// kI8 = true: INT8 cache, 64-token chunks (kmap / vmap over the head-major
+// int8 codes, box {D bytes, 64, 1}; the scales a.k_scales / a.v_scales come
+// in by plain bulk copies).
 template <int D, int G, bool kI8>
 __global__ void __launch_bounds__(kDecodeThreads) __maxnreg__(decode_max_regs<G>())
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap, DecodeArgs a) {
   constexpr int kPanels = D / 64;
   constexpr int kStages = kStagesOf<kI8>;
-  constexpr uint32_t kChunkBytes = kDecodeChunk * D * (kI8 ? 1 : 2);
+  constexpr int kChunk = kChunkOf<kI8>;  // tokens per chunk
+  constexpr uint32_t kChunkBytes = kChunk * D * (kI8 ? 1 : 2);
   constexpr uint32_t kQBytes = G * D * 2;
   constexpr int kWarps = kDecodeThreads / 32;
 
@@ -567,7 +573,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   const int seg0 = min(static_cast<int>(threadIdx.x) * per, a.num_seqs);
   const int seg1 = min(seg0 + per, a.num_seqs);
   long long mine = 0;
-  for (int s = seg0; s < seg1; ++s) mine += seq_chunks(a, s, max_ctx);
+  for (int s = seg0; s < seg1; ++s) mine += seq_chunks<kChunk>(a, s, max_ctx);
   long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -591,7 +597,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   if (ca < cb && ca >= excl * hkv && ca < (excl + mine) * hkv) {
     long long p = excl;
     for (int s = seg0; s < seg1; ++s) {
-      const int n = seq_chunks(a, s, max_ctx);
+      const int n = seq_chunks<kChunk>(a, s, max_ctx);
       if (ca < (p + n) * hkv) {
         sm.start_seq = s;
         sm.start_base = p;
@@ -603,7 +609,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   if (ca < cb && cb - 1 >= excl * hkv && cb - 1 < (excl + mine) * hkv) {
     long long p = excl;
     for (int s = seg0; s < seg1; ++s) {
-      const int n = seq_chunks(a, s, max_ctx);
+      const int n = seq_chunks<kChunk>(a, s, max_ctx);
       if (cb - 1 < (p + n) * hkv) {
         sm.end_seq = s;
         sm.end_base = p;
@@ -671,8 +677,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int k = k0; k < k0 + n; ++k, ++c) {
           const int st = c % kStages;
           if (!claim(st)) return false;
-          const int tok = a.shared_len + k * kDecodeChunk;
-          const int n_valid = (pbad_ctx || pctx - tok <= 0) ? 0 : min(kDecodeChunk, pctx - tok);
+          const int tok = a.shared_len + k * kChunk;
+          const int n_valid = (pbad_ctx || pctx - tok <= 0) ? 0 : min(kChunk, pctx - tok);
           int id = 0;
           bool bad = pbad_ctx;
           if (n_valid > 0 && !bad) {
@@ -714,14 +720,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             mbar_arrive(fb);  // descriptor only
           } else {
             constexpr uint32_t kRowBytes = D * 2;
-            constexpr uint32_t kScaleBytes = kI8 ? kDecodeChunk * 4 : 0u;
+            constexpr uint32_t kScaleBytes = kI8 ? kChunk * 4 : 0u;
             mbar_arrive_expect_tx(fb, 2 * kChunkBytes + 2 * kScaleBytes +
                                           (k == k0 ? kQBytes : 0u) +
                                           (inf.store_slot >= 0 ? 2 * kRowBytes : 0u));
             if constexpr (kI8) {
               // Head-major INT8 blocks: the chunk's codes of this KV head are
-              // one contiguous 32 x D tile (rows of (block, head) = id * Hkv
-              // + kvh), and its 32 scales 128 contiguous bytes.
+              // one contiguous 64 x D tile (rows of (block, head) = id * Hkv
+              // + kvh), and its 64 scales 256 contiguous bytes.
               const int bh = id * a.num_kv_heads + kvh;
               tma_load_3d(smem_u32(&sm.k[st][0]), &kmap, fb, 0, tok & (kBlockSize - 1), bh);
               tma_load_3d(smem_u32(&sm.v[st][0]), &vmap, fb, 0, tok & (kBlockSize - 1), bh);
@@ -769,7 +775,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int eseq = sm.end_seq;
           const long long ebase = sm.end_base * hkv;
           const int ectx = a.context_lens[eseq];
-          const int enc = seq_chunks(a, eseq, max_ctx);
+          const int enc = seq_chunks<kChunk>(a, eseq, max_ctx);
           const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
           if (epair_begin + enc > cb && epair_begin > ca) {
             if (!emit_piece(eseq, ebase, ectx, bad_context(a, ectx, max_ctx), enc, epair_begin, cb, 1))
@@ -780,7 +786,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         long long base = sm.start_base * hkv;  // first chunk of seq's pairs
         int ctx = a.context_lens[seq];
         bool ctx_bad = bad_context(a, ctx, max_ctx);
-        int nch = seq_chunks(a, seq, max_ctx);
+        int nch = seq_chunks<kChunk>(a, seq, max_ctx);
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
         int piece = 0;
@@ -799,7 +805,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             base = pair_end;
             ctx = a.context_lens[seq];
             ctx_bad = bad_context(a, ctx, max_ctx);
-            nch = seq_chunks(a, seq, max_ctx);
+            nch = seq_chunks<kChunk>(a, seq, max_ctx);
             if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
           }
         }
@@ -941,241 +947,248 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       const int valid = inf.n_valid;
       bool zeroed = false;
       if ((c % kConsumerWarps) == warp && valid > 0) {
-        // INT8: the K and V scales of this lane's four tokens (mt * 16 +
-        // hf * 8 + g); read for tokens past the context too, but always
-        // selected away there (pool contents may be anything).
-        float ksc[2][2], vsc[2][2];
-        if constexpr (kI8) {
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int tok = mt * 16 + hf * 8 + g;
-              ksc[mt][hf] = sm.ks[st][tok];
-              vsc[mt][hf] = sm.vs[st][tok];
-            }
-        } else {
-          if (valid < kDecodeChunk) {
-            // V rows past the context: zero them (pool contents may be
-            // anything, and 0 x NaN would poison the product).
-            for (int i = lane; i < (kDecodeChunk - valid) * 8 * kPanels; i += 32) {
-              const int pn = i % kPanels;
-              const int rest = i / kPanels;
-              *reinterpret_cast<uint4*>(&sm.v[st][pn][(valid + rest / 8) * 128 + (rest % 8) * 16]) =
-                  make_uint4(0u, 0u, 0u, 0u);
-            }
-            __syncwarp();
-            zeroed = true;
-          }
-          if (inf.store_slot >= 0) {
-            // Fused store: the new token's K and V rows of this KV head replace
-            // the pool rows loaded for its position, and are written to the
-            // cache slot (each pair stores its own head; one 16-byte piece per
-            // lane).
-            constexpr int kPieces = D / 8;
-            if (lane < 2 * kPieces) {
-              const bool is_v = lane >= kPieces;
-              const int ci = is_v ? lane - kPieces : lane;
-              const uint4 x =
-                  *reinterpret_cast<const uint4*>((is_v ? sm.vnew[st] : sm.knew[st]) + ci * 8);
-              uint8_t* tile = is_v ? &sm.v[st][ci / 8][0] : &sm.k[st][ci / 8][0];
-              *reinterpret_cast<uint4*>(tile + sw128_offset(inf.store_row, ci % 8)) = x;
-              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.v_cache : a.k_cache) +
-                                   static_cast<int64_t>(inf.store_slot) * a.num_kv_heads * D +
-                                   static_cast<int64_t>(inf.kvh) * D + ci * 8;
-              *reinterpret_cast<uint4*>(dst) = x;
-            }
-            __syncwarp();
-            zeroed = true;
-          }
-        }
-        // ---- S^T = K q^T: two m-tiles of 16 tokens x NT n-tiles of 8 heads
-        float sc[2][NT][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
-        if constexpr (kI8) {
-          // Codes converted to bf16 exactly in registers: lane (g, cq) reads
-          // four bytes (dimensions 16 ks + 4 cq .. + 3) of token rows g and
-          // g + 8 of each m-tile (conflict-free under the swizzle).
-          const uint8_t* k8 = sm.k[st];
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-              const int r0 = mt * 16 + g;
-              const uint32_t w0 =
-                  *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0, ks) + 4 * cq) ^
-                  0x80808080u;
-              const uint32_t w1 =
-                  *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0 + 8, ks) + 4 * cq) ^
-                  0x80808080u;
-              uint32_t af[4];
-              af[0] = i8_b01_f16x2(w0);
-              af[2] = i8_b23_f16x2(w0);
-              af[1] = i8_b01_f16x2(w1);
-              af[3] = i8_b23_f16x2(w1);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_16816_f16(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
-            }
-          }
-        } else {
-          const uint32_t kb = smem_u32(&sm.k[st][0][0]);
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-              uint32_t af[4];
-              ldsm_x4(kb + (ks >> 2) * kPanelBytes +
-                          sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
-                      af);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_16816(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
-            }
-          }
-        }
-        // INT8: the running maximum of the piece's V scales (valid tokens;
-        // the eight row groups hold the chunk's tokens).  When it grows the
-        // accumulator, kept in units of it, is rescaled with the softmax's
-        // alpha below.
-        float vfix = 1.f, inv_vs = 0.f;
-        if constexpr (kI8) {
-          float cm = 0.f;
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-              if (mt * 16 + hf * 8 + g < valid) cm = fmaxf(cm, vsc[mt][hf]);
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
-          cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
-          if (cm > vs_ref) {
-            vfix = vs_ref / cm;
-            vs_ref = cm;
-          }
-          inv_vs = vs_ref > 0.f ? 1.f / vs_ref : 0.f;
-        }
-        // ---- online softmax per head (a head's 32 scores sit in the lanes
-        // with the same cq: two per m-tile in each of the 8 row groups)
-        float alpha[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            float mx = -INFINITY;
-#pragma unroll
+        // A chunk of 64 INT8 tokens is taken as two halves of 32, each by
+        // the 32-token step below (one online-softmax update per half); a
+        // bf16 chunk is one such step.
+#pragma unroll 1
+        for (int hoff = 0; hoff < kChunk && hoff < valid; hoff += kDecodeChunk) {
+          const int hvalid = min(valid - hoff, kDecodeChunk);  // tokens of this half
+          // INT8: the K and V scales of this lane's four tokens (mt * 16 +
+          // hf * 8 + g); read for tokens past the context too, but always
+          // selected away there (pool contents may be anything).
+          float ksc[2][2], vsc[2][2];
+          if constexpr (kI8) {
+  #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
+  #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 const int tok = mt * 16 + hf * 8 + g;
-                const float sx = kI8 ? qscale * ksc[mt][hf] * qmul[nt][j] : qscale;
-                const float x = tok < valid ? sc[mt][nt][hf * 2 + j] * sx : -INFINITY;
-                sc[mt][nt][hf * 2 + j] = x;
-                mx = fmaxf(mx, x);
+                ksc[mt][hf] = sm.ks[st][hoff + tok];
+                vsc[mt][hf] = sm.vs[st][hoff + tok];
               }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[nt][j], mx);  // finite: valid > 0
-            alpha[nt][j] = fast_exp2(m_run[nt][j] - m_new);
-            m_run[nt][j] = m_new;
-            float ls = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const float pv = fast_exp2(sc[mt][nt][hf * 2 + j] - m_new);
-                ls += pv;
-                // INT8: P V = vs_ref sum_t (p_t vscale_t / vs_ref) code_t,
-                // with p_t vscale_t / vs_ref <= 1 in f16; the sum keeps p_t.
-                const int tok = mt * 16 + hf * 8 + g;
-                sc[mt][nt][hf * 2 + j] =
-                    kI8 ? (tok < valid ? pv * (vsc[mt][hf] * inv_vs) : 0.f) : pv;
+          } else {
+            if (hvalid < kDecodeChunk) {
+              // V rows past the context: zero them (pool contents may be
+              // anything, and 0 x NaN would poison the product).
+              for (int i = lane; i < (kDecodeChunk - hvalid) * 8 * kPanels; i += 32) {
+                const int pn = i % kPanels;
+                const int rest = i / kPanels;
+                *reinterpret_cast<uint4*>(&sm.v[st][pn][(hvalid + rest / 8) * 128 + (rest % 8) * 16]) =
+                    make_uint4(0u, 0u, 0u, 0u);
               }
-            l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + ls;
-            if constexpr (kI8) alpha[nt][j] *= vfix;
+              __syncwarp();
+              zeroed = true;
+            }
+            if (inf.store_slot >= 0) {
+              // Fused store: the new token's K and V rows of this KV head replace
+              // the pool rows loaded for its position, and are written to the
+              // cache slot (each pair stores its own head; one 16-byte piece per
+              // lane).
+              constexpr int kPieces = D / 8;
+              if (lane < 2 * kPieces) {
+                const bool is_v = lane >= kPieces;
+                const int ci = is_v ? lane - kPieces : lane;
+                const uint4 x =
+                    *reinterpret_cast<const uint4*>((is_v ? sm.vnew[st] : sm.knew[st]) + ci * 8);
+                uint8_t* tile = is_v ? &sm.v[st][ci / 8][0] : &sm.k[st][ci / 8][0];
+                *reinterpret_cast<uint4*>(tile + sw128_offset(inf.store_row, ci % 8)) = x;
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_v ? a.v_cache : a.k_cache) +
+                                     static_cast<int64_t>(inf.store_slot) * a.num_kv_heads * D +
+                                     static_cast<int64_t>(inf.kvh) * D + ci * 8;
+                *reinterpret_cast<uint4*>(dst) = x;
+              }
+              __syncwarp();
+              zeroed = true;
+            }
           }
-        }
-#pragma unroll
-        for (int md = 0; md < KS; ++md)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            o[md][nt][0] *= alpha[nt][0];
-            o[md][nt][1] *= alpha[nt][1];
-            o[md][nt][2] *= alpha[nt][0];
-            o[md][nt][3] *= alpha[nt][1];
-          }
-        // ---- P^T operand fragments: the S^T accumulator of tokens
-        // mt*16 + (0..7 | 8..15) is an 8x8 16-bit matrix per lane pair of
-        // columns; its transpose is the operand layout (bf16, or f16 for
-        // INT8).
-        uint32_t pb[2][NT][2];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            pb[mt][nt][0] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][0], sc[mt][nt][1])
-                                                : pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
-            pb[mt][nt][1] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][2], sc[mt][nt][3])
-                                                : pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
-          }
-        // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, two k-steps of 16 tokens
-        if constexpr (kI8) {
-          // Lane (g, cq) reads four bytes (dimensions 4 (g + 8 p) .. + 3) of
-          // token rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 of the k-step and
-          // pairs the tokens per dimension; dimension 4 (g + 8 p) + e is row
-          // g + 8 (e & 1) of m-tile 2 p + (e >> 1) (the output rows are put
-          // back in order when the state is posted).
-          const uint8_t* v8 = sm.v[st];
-#pragma unroll
-          for (int kt = 0; kt < 2; ++kt) {
-            const int t0 = kt * 16 + 2 * cq;
-#pragma unroll
-            for (int p = 0; p < D / 32; ++p) {
-              const int ch = (g >> 2) + 2 * p;
-              const int wo = 4 * (g & 3);
-              const uint32_t x0 =
-                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0, ch) + wo) ^ 0x80808080u;
-              const uint32_t x1 =
-                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 1, ch) + wo) ^
-                  0x80808080u;
-              const uint32_t x2 =
-                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 8, ch) + wo) ^
-                  0x80808080u;
-              const uint32_t x3 =
-                  *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 9, ch) + wo) ^
-                  0x80808080u;
-              // Token pairs (t0, t0 + 1) and (t0 + 8, t0 + 9) per byte e.
-              uint32_t lo01[2], lo23[2], hi01[2], hi23[2];
-              i8_cross_f16x2(x0, x1, lo01, lo23);
-              i8_cross_f16x2(x2, x3, hi01, hi23);
-              const uint32_t af0[4] = {lo01[0], lo01[1], hi01[0], hi01[1]};  // e = 0, 1
-              const uint32_t af1[4] = {lo23[0], lo23[1], hi23[0], hi23[1]};  // e = 2, 3
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                mma_16816_f16(o[2 * p][nt], af0, pb[kt][nt][0], pb[kt][nt][1]);
-                mma_16816_f16(o[2 * p + 1][nt], af1, pb[kt][nt][0], pb[kt][nt][1]);
+          // ---- S^T = K q^T: two m-tiles of 16 tokens x NT n-tiles of 8 heads
+          float sc[2][NT][4];
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+          if constexpr (kI8) {
+            // Codes converted to bf16 exactly in registers: lane (g, cq) reads
+            // four bytes (dimensions 16 ks + 4 cq .. + 3) of token rows g and
+            // g + 8 of each m-tile (conflict-free under the swizzle).
+            const uint8_t* k8 = sm.k[st] + hoff * D;
+  #pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+  #pragma unroll
+              for (int mt = 0; mt < 2; ++mt) {
+                const int r0 = mt * 16 + g;
+                const uint32_t w0 =
+                    *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0, ks) + 4 * cq) ^
+                    0x80808080u;
+                const uint32_t w1 =
+                    *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0 + 8, ks) + 4 * cq) ^
+                    0x80808080u;
+                uint32_t af[4];
+                af[0] = i8_b01_f16x2(w0);
+                af[2] = i8_b23_f16x2(w0);
+                af[1] = i8_b01_f16x2(w1);
+                af[3] = i8_b23_f16x2(w1);
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma_16816_f16(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
+              }
+            }
+          } else {
+            const uint32_t kb = smem_u32(&sm.k[st][0][0]);
+  #pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+  #pragma unroll
+              for (int mt = 0; mt < 2; ++mt) {
+                uint32_t af[4];
+                ldsm_x4(kb + (ks >> 2) * kPanelBytes +
+                            sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
+                        af);
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma_16816(sc[mt][nt], af, qb[ks][nt][0], qb[ks][nt][1]);
               }
             }
           }
-        } else {
-          const uint32_t vb = smem_u32(&sm.v[st][0][0]);
-#pragma unroll
-          for (int kt = 0; kt < 2; ++kt) {
-#pragma unroll
-            for (int md = 0; md < KS; ++md) {
-              uint32_t af[4];
-              ldsm_x4_trans(vb + (md >> 2) * kPanelBytes +
-                                sw128_offset(kt * 16 + (li >> 1) * 8 + lr, (md & 3) * 2 + (li & 1)),
-                            af);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma_16816(o[md][nt], af, pb[kt][nt][0], pb[kt][nt][1]);
+          // INT8: the running maximum of the piece's V scales (valid tokens;
+          // the eight row groups hold the chunk's tokens).  When it grows the
+          // accumulator, kept in units of it, is rescaled with the softmax's
+          // alpha below.
+          float vfix = 1.f, inv_vs = 0.f;
+          if constexpr (kI8) {
+            float cm = 0.f;
+  #pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                if (mt * 16 + hf * 8 + g < hvalid) cm = fmaxf(cm, vsc[mt][hf]);
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 4));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 8));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+            if (cm > vs_ref) {
+              vfix = vs_ref / cm;
+              vs_ref = cm;
+            }
+            inv_vs = vs_ref > 0.f ? 1.f / vs_ref : 0.f;
+          }
+          // ---- online softmax per head (a head's 32 scores sit in the lanes
+          // with the same cq: two per m-tile in each of the 8 row groups)
+          float alpha[NT][2];
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+  #pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float mx = -INFINITY;
+  #pragma unroll
+              for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                  const int tok = mt * 16 + hf * 8 + g;
+                  const float sx = kI8 ? qscale * ksc[mt][hf] * qmul[nt][j] : qscale;
+                  const float x = tok < hvalid ? sc[mt][nt][hf * 2 + j] * sx : -INFINITY;
+                  sc[mt][nt][hf * 2 + j] = x;
+                  mx = fmaxf(mx, x);
+                }
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+              mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+              const float m_new = fmaxf(m_run[nt][j], mx);  // finite: hvalid > 0
+              alpha[nt][j] = fast_exp2(m_run[nt][j] - m_new);
+              m_run[nt][j] = m_new;
+              float ls = 0.f;
+  #pragma unroll
+              for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                  const float pv = fast_exp2(sc[mt][nt][hf * 2 + j] - m_new);
+                  ls += pv;
+                  // INT8: P V = vs_ref sum_t (p_t vscale_t / vs_ref) code_t,
+                  // with p_t vscale_t / vs_ref <= 1 in f16; the sum keeps p_t.
+                  const int tok = mt * 16 + hf * 8 + g;
+                  sc[mt][nt][hf * 2 + j] =
+                      kI8 ? (tok < hvalid ? pv * (vsc[mt][hf] * inv_vs) : 0.f) : pv;
+                }
+              l_run[nt][j] = l_run[nt][j] * alpha[nt][j] + ls;
+              if constexpr (kI8) alpha[nt][j] *= vfix;
+            }
+          }
+  #pragma unroll
+          for (int md = 0; md < KS; ++md)
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[md][nt][0] *= alpha[nt][0];
+              o[md][nt][1] *= alpha[nt][1];
+              o[md][nt][2] *= alpha[nt][0];
+              o[md][nt][3] *= alpha[nt][1];
+            }
+          // ---- P^T operand fragments: the S^T accumulator of tokens
+          // mt*16 + (0..7 | 8..15) is an 8x8 16-bit matrix per lane pair of
+          // columns; its transpose is the operand layout (bf16, or f16 for
+          // INT8).
+          uint32_t pb[2][NT][2];
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              pb[mt][nt][0] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][0], sc[mt][nt][1])
+                                                  : pack_bf16x2(sc[mt][nt][0], sc[mt][nt][1]));
+              pb[mt][nt][1] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][2], sc[mt][nt][3])
+                                                  : pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
+            }
+          // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, two k-steps of 16 tokens
+          if constexpr (kI8) {
+            // Lane (g, cq) reads four bytes (dimensions 4 (g + 8 p) .. + 3) of
+            // token rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 of the k-step and
+            // pairs the tokens per dimension; dimension 4 (g + 8 p) + e is row
+            // g + 8 (e & 1) of m-tile 2 p + (e >> 1) (the output rows are put
+            // back in order when the state is posted).
+            const uint8_t* v8 = sm.v[st] + hoff * D;
+  #pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+              const int t0 = kt * 16 + 2 * cq;
+  #pragma unroll
+              for (int p = 0; p < D / 32; ++p) {
+                const int ch = (g >> 2) + 2 * p;
+                const int wo = 4 * (g & 3);
+                const uint32_t x0 =
+                    *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0, ch) + wo) ^ 0x80808080u;
+                const uint32_t x1 =
+                    *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 1, ch) + wo) ^
+                    0x80808080u;
+                const uint32_t x2 =
+                    *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 8, ch) + wo) ^
+                    0x80808080u;
+                const uint32_t x3 =
+                    *reinterpret_cast<const uint32_t*>(v8 + i8_offset<D>(t0 + 9, ch) + wo) ^
+                    0x80808080u;
+                // Token pairs (t0, t0 + 1) and (t0 + 8, t0 + 9) per byte e.
+                uint32_t lo01[2], lo23[2], hi01[2], hi23[2];
+                i8_cross_f16x2(x0, x1, lo01, lo23);
+                i8_cross_f16x2(x2, x3, hi01, hi23);
+                const uint32_t af0[4] = {lo01[0], lo01[1], hi01[0], hi01[1]};  // e = 0, 1
+                const uint32_t af1[4] = {lo23[0], lo23[1], hi23[0], hi23[1]};  // e = 2, 3
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  mma_16816_f16(o[2 * p][nt], af0, pb[kt][nt][0], pb[kt][nt][1]);
+                  mma_16816_f16(o[2 * p + 1][nt], af1, pb[kt][nt][0], pb[kt][nt][1]);
+                }
+              }
+            }
+          } else {
+            const uint32_t vb = smem_u32(&sm.v[st][0][0]);
+  #pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+  #pragma unroll
+              for (int md = 0; md < KS; ++md) {
+                uint32_t af[4];
+                ldsm_x4_trans(vb + (md >> 2) * kPanelBytes +
+                                  sw128_offset(kt * 16 + (li >> 1) * 8 + lr, (md & 3) * 2 + (li & 1)),
+                              af);
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma_16816(o[md][nt], af, pb[kt][nt][0], pb[kt][nt][1]);
+              }
             }
           }
         }

@@ -171,15 +171,15 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
 
 // Tensor maps over INT8 codes [num_blocks][Hkv][256][D] bytes viewed as 3-D
 // {D, 256, num_blocks * Hkv}; a box of `rows` consecutive tokens of one
-// (block, KV head) is one contiguous tile.  The decode takes 32 rows with the
-// 128-byte swizzle for D = 128 and 64-byte for D = 64 (the swizzle span is
-// the row); the prefill takes 64 rows unswizzled (its producers dequantise
-// them with plain loads).
+// (block, KV head) is one contiguous tile.  The decode takes 64 rows (one
+// INT8 chunk) with the 128-byte swizzle for D = 128 and 64-byte for D = 64
+// (the swizzle span is the row); the prefill takes 64 rows unswizzled (its
+// producers dequantise them with plain loads).
 bool encode_int8_maps(CUtensorMap* kmap, CUtensorMap* vmap, const void* k, const void* v,
                       int64_t num_blocks, int hkv, int d, bool prefill = false) {
   const uint64_t tiles = static_cast<uint64_t>(num_blocks) * hkv;
   const uint64_t blk = pkv::kBlockSize;
-  const uint32_t rows = prefill ? pkv::kPrefillKeyTile : pkv::kDecodeChunk;
+  const uint32_t rows = prefill ? pkv::kPrefillKeyTile : 2 * pkv::kDecodeChunk;
   const CUtensorMapSwizzle swz = prefill    ? CU_TENSOR_MAP_SWIZZLE_NONE
                                  : d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                             : CU_TENSOR_MAP_SWIZZLE_64B;

@@ -174,9 +174,10 @@ int decode_num_ctas(int head_dim, int group, int num_sms, int64_t num_pairs, int
 size_t decode_counter_bytes(int64_t num_pairs);
 size_t decode_partial_bytes(int num_ctas, int group, int head_dim);
 cudaError_t launch_decode(const DecodeArgs& a, const CacheMaps& maps, cudaStream_t stream);
-// The same split-K decode over an INT8 cache: kmap / vmap view the codes as
-// uint8 {D, 256, num_blocks * Hkv} with box {D, 32, 1} (128-byte swizzle for
-// D = 128, 64-byte for D = 64); a.k_scales / a.v_scales are set.
+// The same split-K decode over an INT8 cache, in chunks of 64 tokens: kmap /
+// vmap view the codes as uint8 {D, 256, num_blocks * Hkv} with box {D, 64, 1}
+// (128-byte swizzle for D = 128, 64-byte for D = 64); a.k_scales /
+// a.v_scales are set.
 cudaError_t launch_decode_i8(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                              cudaStream_t stream);
 
