@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("5b22813f6f6e850f953f6c0d58a10ea65edc82c249d491eb09ccddddfa5be5b5", MAIN_WORKLOAD,
-                      324841216 + 4046080),
+    "decode_append": ("752926de712b9713a1d329ef5a5308123af9dd620dcb6212ddf7266894d6bea8", MAIN_WORKLOAD,
+                      324845056 + 4046080),
 }
 
 
