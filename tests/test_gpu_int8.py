@@ -111,6 +111,16 @@ def test_int8_geometries(cuda_device, d, hq, hkv):
     check_case(case)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_int8_chunk_and_block_edges(cuda_device, d):
+    """Contexts on either side of the 32-token half-chunk, the 64-token INT8
+    chunk and the 256-token block edges (the last chunk partly or wholly
+    past the context, a half with no token)."""
+    lens = [1, 31, 32, 33, 63, 64, 65, 96, 127, 128, 129, 255, 256, 257, 511, 513]
+    case = W.make_decode_case("edge8", lens, 16, 8, d, 40, seed=80 + d)
+    check_case(case)
+
+
 def test_int8_long_contexts(cuda_device):
     case = W.make_decode_case("long8", [9000, 4097, 31], 16, 8, 128, 64, seed=77)
     check_case(case)
