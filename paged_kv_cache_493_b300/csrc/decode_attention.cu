@@ -660,19 +660,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         return (c & 7) != 0 || *reinterpret_cast<volatile int*>(&sm.abort_flag) == 0;
       };
 
-      // Emits the chunks [pos, piece_end) of one piece of sequence pseq (its
-      // pairs start at chunk pbase, pnch chunks each); false on abort.
-      auto emit_piece = [&](int pseq, long long pbase, int pctx, bool pbad_ctx, int pnch,
-                            long long pos, long long piece_end, int slot) -> bool {
-        const int kvh = static_cast<int>((pos - pbase) / pnch);
-        const int k0 = static_cast<int>((pos - pbase) % pnch);
-        const long long pair_end = pbase + static_cast<long long>(kvh + 1) * pnch;
-        const int n = static_cast<int>(piece_end - pos);
-        const bool whole = k0 == 0 && piece_end == pair_end;
+      // Emits one piece of sequence pseq: the chunks [k0, k0 + n) of its pair
+      // kvh (pnch chunks, ending at chunk pair_end of the whole stream) up to
+      // chunk piece_end; false on abort.
+      auto emit_piece = [&](int pseq, int pctx, bool pbad_ctx, int pnch, int kvh, int k0,
+                            long long pair_end, long long piece_end, int slot) -> bool {
         const long long pair_begin = pair_end - pnch;
-        const int c_first = block_of_chunk(pair_begin, T, nb);
-        const int c_last = block_of_chunk(pair_end - 1, T, nb);
-        const int first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
+        const int n = static_cast<int>(piece_end - pair_begin) - k0;
+        const bool whole = k0 == 0 && piece_end == pair_end;
+        // The blocks holding the pair's first and last chunk, and the partial
+        // slot of its piece in the first: the cross-block merge's bookkeeping,
+        // needed only for a cut pair (a whole pair's output is written by the
+        // merger directly).
+        int c_first = static_cast<int>(blockIdx.x), c_last = c_first, first_slot = 0;
+        if (!whole) {
+          c_first = block_of_chunk(pair_begin, T, nb);
+          c_last = block_of_chunk(pair_end - 1, T, nb);
+          first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
+        }
         const int32_t* table = a.block_tables + static_cast<int64_t>(pseq) * a.max_blocks;
         for (int k = k0; k < k0 + n; ++k, ++c) {
           const int st = c % kStages;
@@ -778,7 +783,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int enc = seq_chunks<kChunk>(a, eseq, max_ctx);
           const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
           if (epair_begin + enc > cb && epair_begin > ca) {
-            if (!emit_piece(eseq, ebase, ectx, bad_context(a, ectx, max_ctx), enc, epair_begin, cb, 1))
+            if (!emit_piece(eseq, ectx, bad_context(a, ectx, max_ctx), enc,
+                            static_cast<int>((epair_begin - ebase) / enc), 0, epair_begin + enc, cb,
+                            1))
               aborted = true;
             stop = epair_begin;
           }
@@ -789,24 +796,34 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         int nch = seq_chunks<kChunk>(a, seq, max_ctx);
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
+        // The pair of chunk pos, and pos's offset in it: divided out once,
+        // then carried along (every piece after the first starts a pair).
+        int kvh = static_cast<int>((pos - base) / nch);
+        int k0 = static_cast<int>(pos - base) - kvh * nch;
         int piece = 0;
         while (pos < stop && !aborted) {
-          const int kvh = static_cast<int>((pos - base) / nch);
           const long long pair_end = base + static_cast<long long>(kvh + 1) * nch;
           const long long piece_end = pair_end < stop ? pair_end : stop;
-          if (!emit_piece(seq, base, ctx, ctx_bad, nch, pos, piece_end, piece == 0 ? 0 : 1)) {
+          if (!emit_piece(seq, ctx, ctx_bad, nch, kvh, k0, pair_end, piece_end,
+                          piece == 0 ? 0 : 1)) {
             aborted = true;
             break;
           }
           pos = piece_end;
           ++piece;
-          if (pos == pair_end && kvh + 1 == hkv && pos < stop) {  // next sequence
-            ++seq;
-            base = pair_end;
-            ctx = a.context_lens[seq];
-            ctx_bad = bad_context(a, ctx, max_ctx);
-            nch = seq_chunks<kChunk>(a, seq, max_ctx);
-            if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
+          k0 = 0;
+          if (pos == pair_end) {
+            if (kvh + 1 < hkv) {
+              ++kvh;
+            } else if (pos < stop) {  // next sequence
+              ++seq;
+              base = pair_end;
+              kvh = 0;
+              ctx = a.context_lens[seq];
+              ctx_bad = bad_context(a, ctx, max_ctx);
+              nch = seq_chunks<kChunk>(a, seq, max_ctx);
+              if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
+            }
           }
         }
       }
