@@ -319,10 +319,13 @@ __device__ __forceinline__ bool bad_context(const DecodeArgs& a, int ctx, int ma
 // tokens this kernel streams), and 1 for an empty private part or a rejected
 // context (that chunk carries no tokens).
 template <int kChunk>
-__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int max_ctx) {
-  const int ctx = a.context_lens[s];
+__device__ __forceinline__ int ctx_chunks(const DecodeArgs& a, int ctx, int max_ctx) {
   const int priv = ctx - a.shared_len;
   return (bad_context(a, ctx, max_ctx) || priv <= 0) ? 1 : (priv + kChunk - 1) / kChunk;
+}
+template <int kChunk>
+__device__ __forceinline__ int seq_chunks(const DecodeArgs& a, int s, int max_ctx) {
+  return ctx_chunks<kChunk>(a, a.context_lens[s], max_ctx);
 }
 
 // The partial slot of the piece of a cut pair held by block cb2 (the pair
@@ -679,6 +682,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
         }
         const int32_t* table = a.block_tables + static_cast<int64_t>(pseq) * a.max_blocks;
+        const int32_t* stab = tab_smem ? sm.slice_tab + (pseq - tab_seq0) * a.max_blocks : table;
         for (int k = k0; k < k0 + n; ++k, ++c) {
           const int st = c % kStages;
           if (!claim(st)) return false;
@@ -687,8 +691,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           int id = 0;
           bool bad = pbad_ctx;
           if (n_valid > 0 && !bad) {
-            id = tab_smem ? sm.slice_tab[(pseq - tab_seq0) * a.max_blocks + (tok >> 8)]
-                          : table[tok >> 8];
+            id = stab[tok >> 8];
             if (id < 0 || id >= a.num_blocks) {
               bad = true;
               report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
@@ -780,7 +783,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int eseq = sm.end_seq;
           const long long ebase = sm.end_base * hkv;
           const int ectx = a.context_lens[eseq];
-          const int enc = seq_chunks<kChunk>(a, eseq, max_ctx);
+          const int enc = ctx_chunks<kChunk>(a, ectx, max_ctx);
           const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
           if (epair_begin + enc > cb && epair_begin > ca) {
             if (!emit_piece(eseq, ectx, bad_context(a, ectx, max_ctx), enc,
@@ -793,7 +796,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         long long base = sm.start_base * hkv;  // first chunk of seq's pairs
         int ctx = a.context_lens[seq];
         bool ctx_bad = bad_context(a, ctx, max_ctx);
-        int nch = seq_chunks<kChunk>(a, seq, max_ctx);
+        int nch = ctx_chunks<kChunk>(a, ctx, max_ctx);
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
         // The pair of chunk pos, and pos's offset in it: divided out once,
@@ -821,7 +824,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               kvh = 0;
               ctx = a.context_lens[seq];
               ctx_bad = bad_context(a, ctx, max_ctx);
-              nch = seq_chunks<kChunk>(a, seq, max_ctx);
+              nch = ctx_chunks<kChunk>(a, ctx, max_ctx);
               if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
             }
           }
