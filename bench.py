@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("752926de712b9713a1d329ef5a5308123af9dd620dcb6212ddf7266894d6bea8", MAIN_WORKLOAD,
-                      324845056 + 4046080),
+    "decode_append": ("b613283bb71728fc722f11270949bbabec8ca21101a663e2418d2a815717d0df", MAIN_WORKLOAD,
+                      324842752 + 4124928),
 }
 
 
