@@ -188,14 +188,16 @@ pkv_status pkv_decode_attention_append(const void* q, int64_t q_row_stride, cons
  * ranges ("units") that run in parallel on the CTAs of one thread-block
  * cluster and are merged through distributed shared memory into one fp32
  * partial state per query row (max, sum, unnormalised output); the split-K
- * decode kernel then streams each sequence's private tokens
- * [256 * shared_blocks, context_lens[s]) only and merges the shared partial
- * state into the output by log-sum-exp.  The result equals
+ * decode kernel, launched to overlap it, streams each sequence's private
+ * tokens [256 * shared_blocks, context_lens[s]) only and merges the shared
+ * partial state into the output by log-sum-exp once the first kernel is
+ * done.  The result equals
  * pkv_decode_attention's up to fp32 rounding (softmax is invariant to how
  * the keys are grouped).  A sequence whose leading table entries differ from
  * row 0's, or whose context is shorter than the shared prefix, gets a zero
  * output and PKV_ERR_DEVICE_CHECK.  Workspace as for pkv_decode_attention
- * (plus the shared partial states, sized by pkv_reserve_workspace too).
+ * (plus the shared partial states and as many private ones, sized by
+ * pkv_reserve_workspace too).
  * Two kernel launches on `stream`.
  */
 pkv_status pkv_decode_attention_shared_prefix(const void* q, int64_t q_row_stride,

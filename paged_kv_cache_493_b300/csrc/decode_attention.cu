@@ -89,6 +89,7 @@ constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum
 constexpr int kDecodeThreads = 7 * 32;
 constexpr int kSliceTable = 1024;  // table entries of a slice's sequences kept in shared memory
 constexpr int kSliceSlots = 256;   // fused store: slots of a slice's sequences kept likewise
+constexpr int kDeferRows = 64;     // cascade decode: rows of whole pairs folded after the stream
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
@@ -204,6 +205,75 @@ __device__ __forceinline__ const float* shared_o_at(const DecodeArgs& a, int seq
           static_cast<int64_t>(seq) * G + h) * D + d;
 }
 
+// Cascade decode, one warp, after the block's stream: folds the shared-prefix
+// partial states (one per row: the cluster merged the units) into the private
+// states the merger set aside for the n pairs of list, and writes their
+// outputs.  Per row, with (Mp, Lp, Op) private and (m, l, Os) shared:
+//   M = max(Mp, m), L = Lp 2^(Mp - M) + l 2^(m - M),
+//   out = (Op 2^(Mp - M) + Os 2^(m - M)) / L.
+// A sequence whose leading table entries are not row 0's, or a row the
+// shared kernel failed on (l < 0), gets zeros (the former is reported).  The
+// lanes take the pairs' table entries, then their rows, then the float4
+// groups of their outputs, so the loads of all the pairs are in flight
+// together.
+template <int D, int G>
+__device__ __noinline__ void fold_deferred(const DecodeArgs& a, const int2* list, int* unshared,
+                                           float2* f, int n, int lane) {
+  const int nsb = a.shared_len / kBlockSize;
+  for (int j = lane; j < n; j += 32) unshared[j] = 0;
+  __syncwarp();
+  for (int i = lane; i < n * nsb; i += 32) {
+    const int j = i / nsb;
+    const int b = i - j * nsb;
+    const int32_t* t = a.block_tables + static_cast<int64_t>(list[j].x) * a.max_blocks;
+    if (__ldg(t + b) != __ldg(a.block_tables + b)) unshared[j] = 1;
+  }
+  __syncwarp();
+  grid_dependency_wait();  // the shared-prefix kernel's partials (see the kernel's start)
+  bool any_unshared = false;
+  for (int r = lane; r < n * G; r += 32) {
+    const int j = r / G;
+    const int h = r - j * G;
+    const int64_t row = static_cast<int64_t>(list[j].y) * a.shared_rows_pad +
+                        static_cast<int64_t>(list[j].x) * G + h;
+    const float2 pv = __ldcg(reinterpret_cast<const float2*>(a.private_ml) + row);
+    const float2 sh = __ldcg(reinterpret_cast<const float2*>(a.shared_ml) + row);
+    const float M = fmaxf(pv.x, sh.x);
+    const bool none = M == -INFINITY;
+    const float fp = (none || pv.x == -INFINITY) ? 0.f : fast_exp2(pv.x - M);
+    const float fsh = (none || sh.x == -INFINITY) ? 0.f : fast_exp2(sh.x - M);
+    const float L = pv.y * fp + sh.y * fsh;
+    any_unshared |= unshared[j] != 0;
+    const float inv = (L > 0.f && !unshared[j] && !(sh.y < 0.f)) ? 1.f / L : 0.f;
+    f[r] = make_float2(fp * inv, fsh * inv);
+  }
+  if (__any_sync(0xffffffffu, any_unshared) && lane == 0)
+    report_error(a.err, kErrDeviceCheck, kSiteDecodeShared);
+  __syncwarp();
+  constexpr int kGroups = D / 4;
+  const int total = n * G * kGroups;
+#pragma unroll 4
+  for (int i = lane; i < total; i += 32) {
+    const int r = i / kGroups;
+    const int d = (i - r * kGroups) * 4;
+    const int j = r / G;
+    const int h = r - j * G;
+    const int seq = list[j].x;
+    const int kvh = list[j].y;
+    const int64_t row = static_cast<int64_t>(kvh) * a.shared_rows_pad +
+                        static_cast<int64_t>(seq) * G + h;
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(a.private_o + row * D + d));
+    const float4 y = __ldcg(reinterpret_cast<const float4*>(a.shared_o + row * D + d));
+    const float2 w = f[r];
+    uint2 packed;
+    packed.x = pack_bf16x2(x.x * w.x + y.x * w.y, x.y * w.x + y.y * w.y);
+    packed.y = pack_bf16x2(x.z * w.x + y.z * w.y, x.w * w.x + y.w * w.y);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) +
+                              (static_cast<int64_t>(seq) * a.num_q_heads + kvh * G + h) * D + d) =
+        packed;
+  }
+}
+
 // The ring's K/V tiles.  bf16: per stage, D / 64 panels of 32 rows x 128
 // bytes (128-byte swizzle).  INT8: per stage, 64 rows x D bytes of codes
 // (128-byte swizzle for D = 128, 64-byte for D = 64) and the 64 tokens'
@@ -298,6 +368,12 @@ struct DecodeSmem : KvTiles<D, kI8> {
   // Cascade decode: fold scratch of the merger and of the merge warp.
   FoldScratch<G> fold_merger;
   FoldScratch<G> fold_merge;
+  // Cascade decode: pairs streamed whole whose private states wait for the
+  // fold after the stream, (seq, kvh); whether each shares the prefix; and
+  // the fold's two factors per row.
+  int2 defer_pair[kDeferRows / G];
+  int defer_unshared[kDeferRows / G];
+  float2 defer_f[kDeferRows];
 };
 
 template <int D, int G, bool kI8 = false>
@@ -428,6 +504,7 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
       }
     }
     if (cascade) {
+      grid_dependency_wait();  // the shared-prefix kernel's partials (see the kernel's start)
 #pragma unroll
       for (int h = 0; h < G; ++h) fold_head<G>(a, inf.seq, inf.kvh, h, Mh[h], Lh[h], f, lane);
       __syncwarp();
@@ -496,6 +573,7 @@ __device__ void merge_pair(const DecodeArgs& a, const StageInfo& inf, long long 
       }
     }
     if (cascade) {
+      grid_dependency_wait();  // the shared-prefix kernel's partials (see the kernel's start)
       fold_head<G>(a, inf.seq, inf.kvh, h, M, L, f, lane);
       __syncwarp();
       fold_acc<D, G>(a, inf.seq, inf.kvh, h, f, acc, lane);
@@ -563,8 +641,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     tma_prefetch_desc(&vmap);
   }
   // Inputs may be written by the previous kernel in the stream: nothing
-  // global is read before this point.
-  grid_dependency_wait();
+  // global is read before this point.  Cascade decode (shared_len > 0): the
+  // previous kernel is the shared-prefix kernel, launched just before by the
+  // same call, and only its partial states are this kernel's inputs from it
+  // (everything else was written before it ran, and it waited for that
+  // itself before letting this grid start).  So the private parts stream
+  // while it runs, and the wait is taken just before those partials are
+  // read (the folds below).
+  if (a.shared_len == 0) grid_dependency_wait();
   grid_dependents_launch();
 
   const int max_ctx = a.max_blocks * kBlockSize;
@@ -1279,6 +1363,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // them:
     //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
     int n_jobs = 0;  // merges handed to the merge warp
+    int n_defer = 0;  // cascade decode: whole pairs set aside for the fold after the stream
     bool gen_seen = false;  // lane 0: the launch generation has been published
     for (int k = 0;; ++k) {
       const bool got = mbar_wait_sleepy(smem_u32(&sm.mail_full), k & 1, a.wait_limit_ns, 200);
@@ -1335,12 +1420,33 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       // The mailbox has been read: let the consumers post again.
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sm.mail_free));
-      // Cascade decode: a whole pair's private state is merged here with the
-      // shared-prefix partial states (log-sum-exp), before the division.
+      // Cascade decode: a whole pair's private state is set aside while the
+      // list has room (the shared-prefix kernel may still be running; the
+      // fold comes after the stream, fold_deferred) ...
+      if (single && a.shared_len > 0 && !bad && a.shared_units == 1 && n_defer < kDeferRows / G) {
+        const int64_t prow0 = static_cast<int64_t>(inf.kvh) * a.shared_rows_pad +
+                              static_cast<int64_t>(inf.seq) * G;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int v = lane + 32 * i;
+          if (v >= kVec) continue;
+          const int hh = (v * 4) / D;
+          const int d = v * 4 - hh * D;
+          *reinterpret_cast<float4*>(a.private_o + (prow0 + hh) * D + d) = res[i];
+        }
+        if (lane < G)
+          *reinterpret_cast<float2*>(a.private_ml + (prow0 + lane) * 2) = make_float2(hM, hL);
+        if (lane == 0) sm.defer_pair[n_defer] = make_int2(inf.seq, inf.kvh);
+        ++n_defer;
+        continue;
+      }
+      // ... else it is merged here with the shared-prefix partial states
+      // (log-sum-exp), before the division.
       const bool unshared = single && a.shared_len > 0 && !shares_prefix(a, inf.seq, lane);
       const bool fold = single && a.shared_len > 0 && !bad && !unshared;
       FoldScratch<G>& fs = sm.fold_merger;
       if (fold) {
+        grid_dependency_wait();  // the shared-prefix kernel's partials (see the kernel's start)
 #pragma unroll 1
         for (int h = 0; h < G; ++h)
           fold_head<G>(a, inf.seq, inf.kvh, h, __shfl_sync(0xffffffffu, hM, h),
@@ -1423,6 +1529,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     if (lane == 0) {  // end marker for the merge warp
       sm.job[n_jobs].flags = kEnd;
       mbar_arrive(smem_u32(&sm.job_full[n_jobs]));
+    }
+    if (n_defer > 0) {
+      __syncwarp();  // lane 0's list entries
+      fold_deferred<D, G>(a, sm.defer_pair, sm.defer_unshared, sm.defer_f, n_defer, lane);
     }
   } else if (warp == kMergeWarp) {
     // ------------------------------------------------------------ merge warp

@@ -269,7 +269,8 @@ pkv_status ensure_shared_workspace(DeviceState* ds, size_t bytes) {
 // shared prefix's key tiles are cut into: a set value, or the most that
 // keep the grid within one CTA per SM (at most 8, the portable cluster
 // size).  The cluster merges its units, so one partial state per row
-// remains: bytes = KV heads x padded rows x (head_dim + 2) fp32.
+// remains: KV heads x padded rows x (head_dim + 2) fp32, and the decode's
+// private states of the same rows after them.
 struct SharedPlan {
   int tiles;     // row tiles
   int units;
@@ -290,8 +291,9 @@ SharedPlan shared_plan(int num_seqs, int hkv, int group, int head_dim, int share
   int u = 1;
   while (u * 2 <= want && u * 2 <= p.key_tiles && u * 2 <= 16) u *= 2;
   p.units = u;
+  // The shared partial states, then as many rows of private states.
   const size_t rows = static_cast<size_t>(hkv) * p.rows_pad;
-  p.bytes = rows * head_dim * sizeof(float) + rows * 2 * sizeof(float);
+  p.bytes = 2 * (rows * head_dim * sizeof(float) + rows * 2 * sizeof(float));
   return p;
 }
 
@@ -640,13 +642,24 @@ pkv_status pkv_decode_attention_shared_prefix(
     st = ensure_shared_workspace(ds, plan.bytes);
     if (st != PKV_OK) return st;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
-    const int num_ctas =
-        pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    int num_ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
+    // The decode starts while the shared-prefix kernel still runs, and each
+    // of that kernel's CTAs holds one decode slot of its SM.  A grid of the
+    // slots left starts whole and streams the private parts meanwhile; a
+    // full grid would leave its last blocks to start, each with a full
+    // slice, only once the shared kernel is done.
+    const int64_t shared_ctas = static_cast<int64_t>(plan.tiles) * plan.units * num_kv_heads;
+    const int64_t free_slots =
+        pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, 0) - shared_ctas;
+    if (free_slots >= ds->num_sms && num_ctas > free_slots) num_ctas = static_cast<int>(free_slots);
     st = ensure_workspace(ds, pkv::decode_partial_bytes(num_ctas, g, head_dim),
                           pkv::decode_counter_bytes(pairs));
     if (st != PKV_OK) return st;
+    const size_t sh_rows = static_cast<size_t>(num_kv_heads) * plan.rows_pad;
     float* sh_o = ds->sh;
-    float* sh_ml = sh_o + static_cast<size_t>(num_kv_heads) * plan.rows_pad * head_dim;
+    float* sh_ml = sh_o + sh_rows * head_dim;
+    float* pv_o = sh_ml + sh_rows * 2;
+    float* pv_ml = pv_o + sh_rows * head_dim;
     const uint64_t wait = static_cast<uint64_t>(g_wait_limit_ns.load());
 
     sp.q = q;
@@ -691,6 +704,8 @@ pkv_status pkv_decode_attention_shared_prefix(
     a.shared_rows_pad = plan.rows_pad;
     a.shared_o = sh_o;
     a.shared_ml = sh_ml;
+    a.private_o = pv_o;
+    a.private_ml = pv_ml;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = timed_launch("shared_prefix", s,
@@ -851,8 +866,8 @@ pkv_status pkv_reserve_workspace(int32_t num_seqs, int32_t num_q_heads, int32_t 
   for (int g = 1; g <= 16; g *= 2) {
     if (num_q_heads % g) continue;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * (num_q_heads / g);
-    // The cascade decode's shared-prefix partials, for a prefix of up to the
-    // whole table width.
+    // The cascade decode's shared-prefix partials and private states, for a
+    // prefix of up to the whole table width.
     shared = std::max(shared, shared_plan(std::max(num_seqs, 1), num_q_heads / g, g, head_dim,
                                           max_blocks_per_seq, ds->num_sms).bytes);
     // The bf16 and INT8 decodes (their grids may differ) share the workspace.

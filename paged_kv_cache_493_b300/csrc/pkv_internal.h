@@ -69,6 +69,12 @@ struct DecodeArgs {
   int shared_rows_pad;
   const float* shared_o;
   const float* shared_ml;
+  // Cascade decode: private states (unnormalised output; running max, sum)
+  // of pairs streamed whole, set aside while the shared-prefix kernel may
+  // still run and folded once the block's stream is done.  Rows as in
+  // shared_o / shared_ml with one unit: kvh * shared_rows_pad + seq * G + h.
+  float* private_o;
+  float* private_ml;
   // Fused store (pkv_decode_attention_append; slot_mapping == nullptr: off):
   // row s of k_new / v_new is sequence s's new token, the one at position
   // context_lens[s] - 1.  The block that streams that position's chunk of

@@ -188,3 +188,17 @@ def test_graph_replays_follow_new_inputs(cuda_device):
         case.q = newq
         assert_close(out, oracle_decode_after_store(case), f"replay {seed}")
     no_device_error()
+
+
+@pytest.mark.parametrize("hq,hkv,seqs", [(32, 2, 700), (16, 2, 1400)])
+def test_many_whole_pairs_per_block(cuda_device, hq, hkv, seqs):
+    """Many short private parts: each decode block streams more whole pairs
+    than it sets aside for the fold after its stream (64 / G of them), so the
+    rest are folded as they come; both kinds match the oracle."""
+    g = torch.Generator().manual_seed(hq + seqs)
+    lens = (256 + torch.randint(1, 41, (seqs,), generator=g)).tolist()
+    case = W.make_decode_case("w", lens, hq, hkv, 64, seqs + 20, seed=606 + hq,
+                              shared_prefix_blocks=1)
+    out = run_cascade(case, 1)
+    assert_close(out, oracle_decode_after_store(case), f"hq={hq} hkv={hkv}")
+    no_device_error()
