@@ -212,13 +212,17 @@ __device__ __forceinline__ const float* shared_o_at(const DecodeArgs& a, int seq
 //   M = max(Mp, m), L = Lp 2^(Mp - M) + l 2^(m - M),
 //   out = (Op 2^(Mp - M) + Os 2^(m - M)) / L.
 // A sequence whose leading table entries are not row 0's, or a row the
-// shared kernel failed on (l < 0), gets zeros (the former is reported).  The
-// lanes take the pairs' table entries, then their rows, then the float4
-// groups of their outputs, so the loads of all the pairs are in flight
-// together.
+// shared kernel failed on (l < 0), gets zeros (the former is reported).  Both
+// outputs of every pair come in by bulk copies into `stage` (the K/V ring,
+// idle once the stream is done; 2 x kDeferRows x D fp32) at once, while the
+// lanes take the pairs' table entries and then their rows' (max, sum).
 template <int D, int G>
 __device__ __noinline__ void fold_deferred(const DecodeArgs& a, const int2* list, int* unshared,
-                                           float2* f, int n, int lane) {
+                                           float2* f, int n, float* stage, uint32_t bar,
+                                           int lane) {
+  // The private rows were written by this warp's lanes: order them before
+  // the bulk copies (async proxy) that read them.
+  asm volatile("fence.proxy.async.global;" ::: "memory");
   const int nsb = a.shared_len / kBlockSize;
   for (int j = lane; j < n; j += 32) unshared[j] = 0;
   __syncwarp();
@@ -230,6 +234,18 @@ __device__ __noinline__ void fold_deferred(const DecodeArgs& a, const int2* list
   }
   __syncwarp();
   grid_dependency_wait();  // the shared-prefix kernel's partials (see the kernel's start)
+  constexpr uint32_t kPairBytes = G * D * sizeof(float);
+  float* so = stage;                     // [n][G][D]: the shared partial outputs
+  float* po = stage + kDeferRows * D;    // [n][G][D]: the private outputs
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, 2u * static_cast<uint32_t>(n) * kPairBytes);
+    for (int j = 0; j < n; ++j) {
+      const int64_t row0 = static_cast<int64_t>(list[j].y) * a.shared_rows_pad +
+                           static_cast<int64_t>(list[j].x) * G;
+      bulk_load(smem_u32(so + j * G * D), a.shared_o + row0 * D, kPairBytes, bar);
+      bulk_load(smem_u32(po + j * G * D), a.private_o + row0 * D, kPairBytes, bar);
+    }
+  }
   bool any_unshared = false;
   for (int r = lane; r < n * G; r += 32) {
     const int j = r / G;
@@ -249,7 +265,14 @@ __device__ __noinline__ void fold_deferred(const DecodeArgs& a, const int2* list
   }
   if (__any_sync(0xffffffffu, any_unshared) && lane == 0)
     report_error(a.err, kErrDeviceCheck, kSiteDecodeShared);
-  __syncwarp();
+  if (!__all_sync(0xffffffffu, mbar_wait(bar, 0, a.wait_limit_ns))) {
+    if (lane == 0) {
+      report_error(a.err, kErrTimeout, kSiteDecodeWaitMerge);
+      mbar_wait(bar, 0, kDrainLimitNs);  // the copies land before the block exits
+    }
+    __syncwarp();
+    return;
+  }
   constexpr int kGroups = D / 4;
   const int total = n * G * kGroups;
 #pragma unroll 4
@@ -260,10 +283,8 @@ __device__ __noinline__ void fold_deferred(const DecodeArgs& a, const int2* list
     const int h = r - j * G;
     const int seq = list[j].x;
     const int kvh = list[j].y;
-    const int64_t row = static_cast<int64_t>(kvh) * a.shared_rows_pad +
-                        static_cast<int64_t>(seq) * G + h;
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(a.private_o + row * D + d));
-    const float4 y = __ldcg(reinterpret_cast<const float4*>(a.shared_o + row * D + d));
+    const float4 x = *reinterpret_cast<const float4*>(po + r * D + d);
+    const float4 y = *reinterpret_cast<const float4*>(so + r * D + d);
     const float2 w = f[r];
     uint2 packed;
     packed.x = pack_bf16x2(x.x * w.x + y.x * w.y, x.y * w.x + y.y * w.y);
@@ -374,6 +395,7 @@ struct DecodeSmem : KvTiles<D, kI8> {
   int2 defer_pair[kDeferRows / G];
   int defer_unshared[kDeferRows / G];
   float2 defer_f[kDeferRows];
+  alignas(8) uint64_t fold_bar;  // their outputs' bulk copies into the ring
 };
 
 template <int D, int G, bool kI8 = false>
@@ -629,6 +651,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     mbar_init(smem_u32(&sm.mail_free), 1);
     mbar_init(smem_u32(&sm.gen_full), 1);
     for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&sm.job_full[j]), 1);
+    mbar_init(smem_u32(&sm.fold_bar), 1);
     sm.abort_flag = 0;
     sm.start_seq = -1;
     sm.start_base = 0;
@@ -1364,6 +1387,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     //   M = max_j m_j, L = sum_j l_j 2^(m_j - M), out = sum_j o_j 2^(m_j - M) / L.
     int n_jobs = 0;  // merges handed to the merge warp
     int n_defer = 0;  // cascade decode: whole pairs set aside for the fold after the stream
+    bool ended = false;  // the consumers' end marker came (the ring is idle)
     bool gen_seen = false;  // lane 0: the launch generation has been published
     for (int k = 0;; ++k) {
       const bool got = mbar_wait_sleepy(smem_u32(&sm.mail_full), k & 1, a.wait_limit_ns, 200);
@@ -1375,7 +1399,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         break;
       }
       const StageInfo inf = sm.mail_info;
-      if (inf.flags & kEnd) break;
+      if (inf.flags & kEnd) {
+        ended = true;
+        break;
+      }
       const bool bad = (inf.flags & kBad) != 0;
       const bool single = (inf.flags & kSingle) != 0;
       const int64_t row_base = static_cast<int64_t>(inf.seq) * a.num_q_heads + inf.kvh * G;
@@ -1423,7 +1450,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       // Cascade decode: a whole pair's private state is set aside while the
       // list has room (the shared-prefix kernel may still be running; the
       // fold comes after the stream, fold_deferred) ...
-      if (single && a.shared_len > 0 && !bad && a.shared_units == 1 && n_defer < kDeferRows / G) {
+      if (!kI8 && single && a.shared_len > 0 && !bad && a.shared_units == 1 &&
+          n_defer < kDeferRows / G) {
         const int64_t prow0 = static_cast<int64_t>(inf.kvh) * a.shared_rows_pad +
                               static_cast<int64_t>(inf.seq) * G;
 #pragma unroll
@@ -1530,9 +1558,16 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       sm.job[n_jobs].flags = kEnd;
       mbar_arrive(smem_u32(&sm.job_full[n_jobs]));
     }
-    if (n_defer > 0) {
-      __syncwarp();  // lane 0's list entries
-      fold_deferred<D, G>(a, sm.defer_pair, sm.defer_unshared, sm.defer_f, n_defer, lane);
+    if constexpr (!kI8) {
+      static_assert(sizeof(KvTiles<D, false>) >= 2 * kDeferRows * D * sizeof(float),
+                    "the ring holds both outputs of kDeferRows rows");
+      if (n_defer > 0 && ended &&
+          !__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&sm.abort_flag), 0)) {
+        __syncwarp();  // lane 0's list entries
+        fold_deferred<D, G>(a, sm.defer_pair, sm.defer_unshared, sm.defer_f, n_defer,
+                            reinterpret_cast<float*>(&sm.k[0][0][0]), smem_u32(&sm.fold_bar),
+                            lane);
+      }
     }
   } else if (warp == kMergeWarp) {
     // ------------------------------------------------------------ merge warp
