@@ -1073,20 +1073,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       piece_bad |= (inf.flags & kBad) != 0;
       const int valid = inf.n_valid;
       bool zeroed = false;
-      if ((c % kConsumerWarps) == warp && valid > 0) {
-        // A chunk of 64 INT8 tokens is taken as two halves of 32, each by
-        // the 32-token step below (one online-softmax update per half); a
-        // bf16 chunk is one such step.
-#pragma unroll 1
-        for (int hoff = 0; hoff < kChunk && hoff < valid; hoff += kDecodeChunk) {
-          const int hvalid = min(valid - hoff, kDecodeChunk);  // tokens of this half
+      // Who computes what.  bf16: warp c % 4 takes the whole 32-token chunk
+      // c in one step of two m-tiles.  INT8: every warp takes its 16 of the
+      // chunk's 64 tokens in one step of one m-tile, so that a stage is done
+      // (and freed for the next copy) four times sooner; the four states
+      // meet in the merger as for bf16.  Per-token work is the same.
+      constexpr int MT = kI8 ? 1 : 2;  // m-tiles (16 tokens) per step
+      constexpr int kStep = 16 * MT;
+      const int hoff = kI8 ? warp * kStep : 0;
+      if ((kI8 || (c % kConsumerWarps) == warp) && valid > hoff) {
+        {
+          const int hvalid = min(valid - hoff, kStep);  // tokens of this step
           // INT8: the K and V scales of this lane's four tokens (mt * 16 +
           // hf * 8 + g); read for tokens past the context too, but always
           // selected away there (pool contents may be anything).
-          float ksc[2][2], vsc[2][2];
+          float ksc[MT][2], vsc[MT][2];
           if constexpr (kI8) {
   #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 const int tok = mt * 16 + hf * 8 + g;
@@ -1097,7 +1101,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             if (hvalid < kDecodeChunk) {
               // V rows past the context: zero them (pool contents may be
               // anything, and 0 x NaN would poison the product).
-              for (int i = lane; i < (kDecodeChunk - hvalid) * 8 * kPanels; i += 32) {
+              for (int i = lane; i < (kStep - hvalid) * 8 * kPanels; i += 32) {
                 const int pn = i % kPanels;
                 const int rest = i / kPanels;
                 *reinterpret_cast<uint4*>(&sm.v[st][pn][(hvalid + rest / 8) * 128 + (rest % 8) * 16]) =
@@ -1128,10 +1132,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               zeroed = true;
             }
           }
-          // ---- S^T = K q^T: two m-tiles of 16 tokens x NT n-tiles of 8 heads
-          float sc[2][NT][4];
+          // ---- S^T = K q^T: MT m-tiles of 16 tokens x NT n-tiles of 8 heads
+          float sc[MT][NT][4];
   #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+          for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
   #pragma unroll
@@ -1144,7 +1148,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
   #pragma unroll
-              for (int mt = 0; mt < 2; ++mt) {
+              for (int mt = 0; mt < MT; ++mt) {
                 const int r0 = mt * 16 + g;
                 const uint32_t w0 =
                     *reinterpret_cast<const uint32_t*>(k8 + i8_offset<D>(r0, ks) + 4 * cq) ^
@@ -1167,7 +1171,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
   #pragma unroll
-              for (int mt = 0; mt < 2; ++mt) {
+              for (int mt = 0; mt < MT; ++mt) {
                 uint32_t af[4];
                 ldsm_x4(kb + (ks >> 2) * kPanelBytes +
                             sw128_offset(mt * 16 + (li & 1) * 8 + lr, (ks & 3) * 2 + (li >> 1)),
@@ -1186,7 +1190,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           if constexpr (kI8) {
             float cm = 0.f;
   #pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
+            for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
               for (int hf = 0; hf < 2; ++hf)
                 if (mt * 16 + hf * 8 + g < hvalid) cm = fmaxf(cm, vsc[mt][hf]);
@@ -1199,7 +1203,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             }
             inv_vs = vs_ref > 0.f ? 1.f / vs_ref : 0.f;
           }
-          // ---- online softmax per head (a head's 32 scores sit in the lanes
+          // ---- online softmax per head (a head's 16 MT scores sit in the lanes
           // with the same cq: two per m-tile in each of the 8 row groups)
           float alpha[NT][2];
   #pragma unroll
@@ -1208,7 +1212,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             for (int j = 0; j < 2; ++j) {
               float mx = -INFINITY;
   #pragma unroll
-              for (int mt = 0; mt < 2; ++mt)
+              for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                   const int tok = mt * 16 + hf * 8 + g;
@@ -1225,7 +1229,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               m_run[nt][j] = m_new;
               float ls = 0.f;
   #pragma unroll
-              for (int mt = 0; mt < 2; ++mt)
+              for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                   const float pv = fast_exp2(sc[mt][nt][hf * 2 + j] - m_new);
@@ -1253,9 +1257,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           // mt*16 + (0..7 | 8..15) is an 8x8 16-bit matrix per lane pair of
           // columns; its transpose is the operand layout (bf16, or f16 for
           // INT8).
-          uint32_t pb[2][NT][2];
+          uint32_t pb[MT][NT][2];
   #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+          for (int mt = 0; mt < MT; ++mt)
   #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               pb[mt][nt][0] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][0], sc[mt][nt][1])
@@ -1263,7 +1267,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               pb[mt][nt][1] = movmatrix_trans(kI8 ? pack_f16x2(sc[mt][nt][2], sc[mt][nt][3])
                                                   : pack_bf16x2(sc[mt][nt][2], sc[mt][nt][3]));
             }
-          // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, two k-steps of 16 tokens
+          // ---- O^T += V^T P^T: D/16 m-tiles of dimensions, MT k-steps of 16 tokens
           if constexpr (kI8) {
             // Lane (g, cq) reads four bytes (dimensions 4 (g + 8 p) .. + 3) of
             // token rows 2 cq, 2 cq + 1, 2 cq + 8, 2 cq + 9 of the k-step and
@@ -1272,7 +1276,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             // back in order when the state is posted).
             const uint8_t* v8 = sm.v[st] + hoff * D;
   #pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
+            for (int kt = 0; kt < MT; ++kt) {
               const int t0 = kt * 16 + 2 * cq;
   #pragma unroll
               for (int p = 0; p < D / 32; ++p) {
@@ -1305,7 +1309,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           } else {
             const uint32_t vb = smem_u32(&sm.v[st][0][0]);
   #pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
+            for (int kt = 0; kt < MT; ++kt) {
   #pragma unroll
               for (int md = 0; md < KS; ++md) {
                 uint32_t af[4];
