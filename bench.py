@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("b613283bb71728fc722f11270949bbabec8ca21101a663e2418d2a815717d0df", MAIN_WORKLOAD,
-                      324842752 + 4124928),
+    "decode_append": ("8e86e66d7e12669d95b13935ac67e88424b762f1fce7d5d1d55e58f4360d4339", MAIN_WORKLOAD,
+                      324843776 + 4054016),
 }
 
 
