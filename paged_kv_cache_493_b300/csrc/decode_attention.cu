@@ -108,8 +108,9 @@ constexpr int kBad = 4;     // the chunk's length or block id is out of range
 constexpr int kSingle = 8;  // the piece is the whole pair: write the output itself
 constexpr int kEnd = 16;    // the slice is done: leave the loop
 
-// The block whose slice holds chunk x when T chunks are cut into nb equal
-// slices (slice c = [c T / nb, (c + 1) T / nb)).
+// The block whose slice holds position x when T cost units are cut into nb
+// equal slices (slice c = [c T / nb, (c + 1) T / nb)); a chunk is one unit,
+// and belongs to the block whose slice holds it.
 __device__ __forceinline__ int block_of_chunk(long long x, long long T, long long nb) {
   return static_cast<int>(((x + 1) * nb - 1) / T);
 }
@@ -677,13 +678,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   const int max_ctx = a.max_blocks * kBlockSize;
   const int hkv = a.num_kv_heads;
 
-  // ---- prefix sums of the chunk counts over the sequences (whole block):
-  // thread t owns sequences [seg0, seg1).
+  // ---- prefix sums of the pairs' costs (pair_gap + chunks) over the
+  // sequences (whole block): thread t owns sequences [seg0, seg1).
   const int per = (a.num_seqs + kDecodeThreads - 1) / kDecodeThreads;
   const int seg0 = min(static_cast<int>(threadIdx.x) * per, a.num_seqs);
   const int seg1 = min(seg0 + per, a.num_seqs);
+  const int gap = a.pair_gap;
   long long mine = 0;
-  for (int s = seg0; s < seg1; ++s) mine += seq_chunks<kChunk>(a, s, max_ctx);
+  for (int s = seg0; s < seg1; ++s) mine += seq_chunks<kChunk>(a, s, max_ctx) + gap;
   long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -698,16 +700,16 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     if (w < warp) before += sm.scan[w];
     total += sm.scan[w];
   }
-  const long long excl = before + incl - mine;  // chunks per KV head before seg0
-  const long long T = total * hkv;              // chunks of all pairs
+  const long long excl = before + incl - mine;  // cost per KV head before seg0
+  const long long T = total * hkv;              // cost of all pairs
   const long long nb = gridDim.x;
   const long long ca = static_cast<long long>(blockIdx.x) * T / nb;        // slice begin
   const long long cb = (static_cast<long long>(blockIdx.x) + 1) * T / nb;  // slice end
-  // The sequences holding the slice's first and last chunks.
+  // The sequences holding the slice's first and last cost units.
   if (ca < cb && ca >= excl * hkv && ca < (excl + mine) * hkv) {
     long long p = excl;
     for (int s = seg0; s < seg1; ++s) {
-      const int n = seq_chunks<kChunk>(a, s, max_ctx);
+      const int n = seq_chunks<kChunk>(a, s, max_ctx) + gap;
       if (ca < (p + n) * hkv) {
         sm.start_seq = s;
         sm.start_base = p;
@@ -719,7 +721,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   if (ca < cb && cb - 1 >= excl * hkv && cb - 1 < (excl + mine) * hkv) {
     long long p = excl;
     for (int s = seg0; s < seg1; ++s) {
-      const int n = seq_chunks<kChunk>(a, s, max_ctx);
+      const int n = seq_chunks<kChunk>(a, s, max_ctx) + gap;
       if (cb - 1 < (p + n) * hkv) {
         sm.end_seq = s;
         sm.end_base = p;
@@ -771,22 +773,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       };
 
       // Emits one piece of sequence pseq: the chunks [k0, k0 + n) of its pair
-      // kvh (pnch chunks, ending at chunk pair_end of the whole stream) up to
-      // chunk piece_end; false on abort.
-      auto emit_piece = [&](int pseq, int pctx, bool pbad_ctx, int pnch, int kvh, int k0,
-                            long long pair_end, long long piece_end, int slot) -> bool {
-        const long long pair_begin = pair_end - pnch;
-        const int n = static_cast<int>(piece_end - pair_begin) - k0;
-        const bool whole = k0 == 0 && piece_end == pair_end;
+      // kvh (pnch chunks; the pair's cost units start at pstart, its chunk 0
+      // sits at pfirst = pstart + pair_gap); false on abort.
+      auto emit_piece = [&](int pseq, int pctx, bool pbad_ctx, int pnch, int kvh, int k0, int n,
+                            long long pfirst, long long pstart, int slot) -> bool {
+        const bool whole = k0 == 0 && n == pnch;
         // The blocks holding the pair's first and last chunk, and the partial
         // slot of its piece in the first: the cross-block merge's bookkeeping,
         // needed only for a cut pair (a whole pair's output is written by the
-        // merger directly).
+        // merger directly).  The piece is that block's first (slot 0) when
+        // its slice holds no chunk of an earlier pair: it starts at or after
+        // the pair's first cost unit (every unit before that, back to the
+        // previous pair's gap, is a chunk of the previous pair).
         int c_first = static_cast<int>(blockIdx.x), c_last = c_first, first_slot = 0;
         if (!whole) {
-          c_first = block_of_chunk(pair_begin, T, nb);
-          c_last = block_of_chunk(pair_end - 1, T, nb);
-          first_slot = slice_begin(c_first, T, nb) == pair_begin ? 0 : 1;
+          c_first = block_of_chunk(pfirst, T, nb);
+          c_last = block_of_chunk(pfirst + pnch - 1, T, nb);
+          first_slot = slice_begin(c_first, T, nb) >= pstart ? 0 : 1;
         }
         const int32_t* table = a.block_tables + static_cast<int64_t>(pseq) * a.max_blocks;
         const int32_t* stab = tab_smem ? sm.slice_tab + (pseq - tab_seq0) * a.max_blocks : table;
@@ -891,36 +894,48 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const long long ebase = sm.end_base * hkv;
           const int ectx = a.context_lens[eseq];
           const int enc = ctx_chunks<kChunk>(a, ectx, max_ctx);
-          const long long epair_begin = ebase + ((cb - 1 - ebase) / enc) * enc;
-          if (epair_begin + enc > cb && epair_begin > ca) {
-            if (!emit_piece(eseq, ectx, bad_context(a, ectx, max_ctx), enc,
-                            static_cast<int>((epair_begin - ebase) / enc), 0, epair_begin + enc, cb,
-                            1))
+          const int epl = enc + gap;  // the pair's cost
+          const long long epair_begin = ebase + ((cb - 1 - ebase) / epl) * epl;
+          const long long efirst = epair_begin + gap;
+          if (epair_begin + epl > cb && epair_begin > ca) {
+            // (none when the slice ends in the pair's gap)
+            if (efirst < cb &&
+                !emit_piece(eseq, ectx, bad_context(a, ectx, max_ctx), enc,
+                            static_cast<int>((epair_begin - ebase) / epl), 0,
+                            static_cast<int>(cb - efirst), efirst, epair_begin, 1))
               aborted = true;
             stop = epair_begin;
           }
         }
-        long long base = sm.start_base * hkv;  // first chunk of seq's pairs
+        long long base = sm.start_base * hkv;  // first cost unit of seq's pairs
         int ctx = a.context_lens[seq];
         bool ctx_bad = bad_context(a, ctx, max_ctx);
         int nch = ctx_chunks<kChunk>(a, ctx, max_ctx);
+        int pl = nch + gap;  // a pair's cost
         if (ctx_bad && base >= ca) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
         long long pos = ca;
-        // The pair of chunk pos, and pos's offset in it: divided out once,
-        // then carried along (every piece after the first starts a pair).
-        int kvh = static_cast<int>((pos - base) / nch);
-        int k0 = static_cast<int>(pos - base) - kvh * nch;
+        // The pair of unit pos, and the first of its chunks at or after pos:
+        // divided out once, then carried along (every piece after the first
+        // starts a pair).
+        int kvh = static_cast<int>((pos - base) / pl);
+        int k0 = max(0, static_cast<int>(pos - base) - kvh * pl - gap);
         int piece = 0;
         while (pos < stop && !aborted) {
-          const long long pair_end = base + static_cast<long long>(kvh + 1) * nch;
+          const long long pair_start = base + static_cast<long long>(kvh) * pl;
+          const long long pair_end = pair_start + pl;
           const long long piece_end = pair_end < stop ? pair_end : stop;
-          if (!emit_piece(seq, ctx, ctx_bad, nch, kvh, k0, pair_end, piece_end,
-                          piece == 0 ? 0 : 1)) {
-            aborted = true;
-            break;
+          // Its chunks in [pos, piece_end): none when the slice stops in the
+          // pair's gap.
+          const int n = static_cast<int>(piece_end - (pair_start + gap)) - k0;
+          if (n > 0) {
+            if (!emit_piece(seq, ctx, ctx_bad, nch, kvh, k0, n, pair_start + gap, pair_start,
+                            piece == 0 ? 0 : 1)) {
+              aborted = true;
+              break;
+            }
+            ++piece;
           }
           pos = piece_end;
-          ++piece;
           k0 = 0;
           if (pos == pair_end) {
             if (kvh + 1 < hkv) {
@@ -932,6 +947,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               ctx = a.context_lens[seq];
               ctx_bad = bad_context(a, ctx, max_ctx);
               nch = ctx_chunks<kChunk>(a, ctx, max_ctx);
+              pl = nch + gap;
               if (ctx_bad) report_error(a.err, kErrDeviceCheck, kSiteDecodeContext);
             }
           }

@@ -45,6 +45,12 @@ struct DecodeArgs {
   // by a slice boundary leaves one partial state per piece; the block that
   // writes the pair's last piece merges them.
   int num_ctas;      // blocks of the decode kernel
+  // The stream is cut into num_ctas equal slices of cost: a pair of nch
+  // chunks costs pair_gap + nch units, the pair_gap units before its first
+  // chunk holding nothing.  pair_gap > 0 charges each piece boundary as
+  // pair_gap chunks, so a block that crosses many short pairs gets fewer
+  // chunks; 0 cuts the chunks evenly.
+  int pair_gap;
   // Counter region (zero when first used, never reset): a 256-byte header
   // (word 0: launch epoch; word 1: blocks finished in this launch) and then
   // one arrival counter per (sequence, KV head) pair, [num_seqs *
