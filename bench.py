@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("8e86e66d7e12669d95b13935ac67e88424b762f1fce7d5d1d55e58f4360d4339", MAIN_WORKLOAD,
-                      324843776 + 4054016),
+    "decode_append": ("9b5489be700607fbd6c60f1d2f91e52abd56ffbe29becbd2285a4c2a2c202dd2", MAIN_WORKLOAD,
+                      324845312 + 4020736),
 }
 
 
