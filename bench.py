@@ -63,7 +63,7 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("9b5489be700607fbd6c60f1d2f91e52abd56ffbe29becbd2285a4c2a2c202dd2", MAIN_WORKLOAD,
+    "decode_append": ("c7443f0ea48763cfd43025dc7e817e2445412baaa3d15b186f20aee24ee8cf45", MAIN_WORKLOAD,
                       324845312 + 4020736),
 }
 

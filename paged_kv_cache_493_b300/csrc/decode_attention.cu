@@ -17,11 +17,12 @@
 //
 // Work structure (stream-K).  Every (sequence, KV head) pair's context is
 // a run of 32-token chunks (an empty or rejected context counts as one
-// chunk, where its zero output is written).  The runs of all pairs, laid end
-// to end, are cut into equal contiguous slices, one per block of a grid that
-// fills the GPU once: every block has the same number of chunks to stream,
-// so all blocks finish together.  Each block computes the prefix sums of the
-// chunk counts over the sequences itself (the lengths live on the device).
+// chunk, where its zero output is written), preceded by pair_gap cost units
+// that hold nothing (what a piece boundary costs, in chunks).  The runs of
+// all pairs, laid end to end, are cut into equal contiguous slices of cost,
+// one per block of a grid that fills the GPU once, so that all blocks
+// finish together.  Each block computes the prefix sums of the costs over
+// the sequences itself (the lengths live on the device).
 // The piece of a pair inside one slice is either the whole pair (its output
 // is written directly) or a cut piece: its partial state goes to one of the
 // block's two partial slots and is counted on the pair's arrival counter;
@@ -41,8 +42,10 @@
 //                 Each stage carries a descriptor (sequence, KV head, slot,
 //                 valid tokens, first / last chunk of the piece); a final
 //                 stage marks the end.
-//   warps 0..3    consumers: warp w computes the chunks c with c % 4 == w
-//                 (and reads every stage's descriptor).  A chunk is two
+//   warps 0..3    consumers: bf16: warp w computes the chunks c with
+//                 c % 4 == w; INT8 (64-token chunks): every warp computes
+//                 its 16 tokens of every chunk.  Each reads every stage's
+//                 descriptor.  A chunk is two
 //                 small contractions on the tensor cores (mma.sync m16n8k16,
 //                 bf16 in, fp32 accumulate): S^T = K q^T with the 32 tokens
 //                 as rows and the G query heads as columns (padded to 8), so
@@ -56,7 +59,9 @@
 //                 and goes on.
 //   warp 5        merger: combines the four warps' states of each posted
 //                 piece, frees the mailbox, then writes a whole pair's output
-//                 or a cut piece's partials and counts it.
+//                 or a cut piece's partials and counts it.  Cascade decode:
+//                 a whole pair's private state is set aside and folded with
+//                 the shared-prefix partials after the stream (fold_deferred).
 //   warp 6        merge warp: merges the pieces of the cut pairs whose count
 //                 this block completed (reads of partials written by other
 //                 blocks: L2 round trips, kept off the consumers' path).
@@ -82,7 +87,7 @@ template <bool kI8>
 constexpr int kChunkOf = kI8 ? 2 * kDecodeChunk : kDecodeChunk;
 template <bool kI8>
 constexpr int kStagesOf = 4;
-constexpr int kConsumerWarps = 4;  // warps 0..3: warp w computes the chunks c with c % 4 == w
+constexpr int kConsumerWarps = 4;  // warps 0..3 (which tokens each computes: see the header)
 constexpr int kProducerWarp = 4;   // TMA issue
 constexpr int kMergerWarp = 5;     // combines the consumers' states, writes results, counts pieces
 constexpr int kMergeWarp = 6;      // merges the pieces of cut contexts (log-sum-exp over L2)
