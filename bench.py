@@ -59,11 +59,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # of the capture: the figure is reported only while the sources still hash to
 # that value (any change to the kernel makes it null until captured again).
 KERNEL_SOURCES = {
-    "decode_append": ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h"),
+    "decode_append": ("decode_attention.cu", "pkv_device.cuh", "pkv_internal.h", "pkv_pair_gap.h"),
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("c7443f0ea48763cfd43025dc7e817e2445412baaa3d15b186f20aee24ee8cf45", MAIN_WORKLOAD,
+    "decode_append": ("5218d014c6d1d98c28dd3248c79cbb12ce3f2e97773255e85ecb4e46773faff8", MAIN_WORKLOAD,
                       324845312 + 4020736),
 }
 

@@ -24,7 +24,7 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "store_kvcache.cu", "decode_attention.cu", "prefill_attention.cu",
            "decode_noalloc.cu", "int8_kv.cu", "block_manager.cpp"]
-HEADERS = [os.path.join(CSRC, h) for h in ("pkv_device.cuh", "pkv_internal.h")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("pkv_device.cuh", "pkv_internal.h", "pkv_pair_gap.h")] + [
     os.path.join(INCLUDE, "pkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

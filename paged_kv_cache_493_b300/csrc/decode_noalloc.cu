@@ -24,6 +24,7 @@
 #include "pkv.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_pair_gap.h"
 
 namespace {
 
@@ -139,6 +140,7 @@ extern "C" pkv_status pkv_decode_attention_noalloc(
   const int g = num_q_heads / num_kv_heads;
   const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
   a.num_ctas = pkv::decode_num_ctas(head_dim, g, num_sms, pairs, pkv::max_splits_setting());
+  a.pair_gap = pkv::kPairGapDecode;
   if (pkv::decode_counter_bytes(pairs) > kCounterBytes ||
       pkv::decode_partial_bytes(a.num_ctas, g, head_dim) > kPartialBytes)
     return PKV_ERR_UNSUPPORTED;

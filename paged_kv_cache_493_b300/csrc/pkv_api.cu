@@ -18,6 +18,7 @@
 #include "pkv.h"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "pkv_pair_gap.h"
 
 namespace {
 
@@ -264,18 +265,6 @@ pkv_status ensure_shared_workspace(DeviceState* ds, size_t bytes) {
   return PKV_OK;
 }
 
-// What a piece boundary costs in the decode's split, in chunks
-// (DecodeArgs::pair_gap): a block crossing more pairs than the others ends
-// last unless each boundary is charged.  Set by measurement on B300:
-// qwen_decode_b128's bf16 step is flat in it (62.4 us at 0, 62.1 at 1); its
-// INT8 decode, whose 64-token chunks make a boundary cost more next to a
-// chunk, goes from 53.2 us at 0 to 49.5 at 1 (50.9 at 2); the cascade's
-// private parts are a few chunks per pair, and prefix_decode_b64 is best at
-// 2 (31.6-32.8 us, against 32.7-32.9 at 0 and 1, 34.4 at 4).
-constexpr int kPairGapDecode = 1;
-constexpr int kPairGapInt8 = 1;
-constexpr int kPairGapCascade = 2;
-
 // Cascade decode plan: row tiles of 128 / G sequences, and the units (one
 // cluster of CTAs per row tile and KV head, a power of two up to 16) the
 // shared prefix's key tiles are cut into: a set value, or the most that
@@ -489,7 +478,7 @@ pkv_status pkv_decode_attention_int8(const void* q, int64_t q_row_stride, const 
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
     a.num_ctas =
         pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load(), true);
-    a.pair_gap = kPairGapInt8;
+    a.pair_gap = pkv::kPairGapInt8;
     st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
                           pkv::decode_counter_bytes(pairs));
     if (st != PKV_OK) return st;
@@ -540,7 +529,7 @@ pkv_status pkv_decode_attention(const void* q, int64_t q_row_stride, const void*
     const int g = num_q_heads / num_kv_heads;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
     a.num_ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
-    a.pair_gap = kPairGapDecode;
+    a.pair_gap = pkv::kPairGapDecode;
     st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
                           pkv::decode_counter_bytes(pairs));
     if (st != PKV_OK) return st;
@@ -598,7 +587,7 @@ pkv_status pkv_decode_attention_append(const void* q, int64_t q_row_stride, cons
     const int g = num_q_heads / num_kv_heads;
     const int64_t pairs = static_cast<int64_t>(num_seqs) * num_kv_heads;
     a.num_ctas = pkv::decode_num_ctas(head_dim, g, ds->num_sms, pairs, g_max_splits.load());
-    a.pair_gap = kPairGapDecode;
+    a.pair_gap = pkv::kPairGapDecode;
     st = ensure_workspace(ds, pkv::decode_partial_bytes(a.num_ctas, g, head_dim),
                           pkv::decode_counter_bytes(pairs));
     if (st != PKV_OK) return st;
@@ -711,7 +700,7 @@ pkv_status pkv_decode_attention_shared_prefix(
     a.wait_limit_ns = wait;
     a.err = ds->err;
     a.num_ctas = num_ctas;
-    a.pair_gap = kPairGapCascade;
+    a.pair_gap = pkv::kPairGapCascade;
     a.counters = ds->cnt;
     a.part_o = ds->ws;
     a.part_ml = a.part_o + static_cast<size_t>(num_ctas) * 2 * g * head_dim;
