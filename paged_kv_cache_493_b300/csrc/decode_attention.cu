@@ -95,6 +95,7 @@ constexpr int kDecodeThreads = 7 * 32;
 constexpr int kSliceTable = 1024;  // table entries of a slice's sequences kept in shared memory
 constexpr int kSliceSlots = 256;   // fused store: slots of a slice's sequences kept likewise
 constexpr int kDeferRows = 64;     // cascade decode: rows of whole pairs folded after the stream
+constexpr int kPrefetchLines = 256;  // L2 prefetch of the tables per block, in 128-byte lines
 
 // Descriptor of one ring stage, written by the producer before it arrives
 // on the stage's full barrier.
@@ -680,6 +681,22 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   if (a.shared_len == 0) grid_dependency_wait();
   grid_dependents_launch();
 
+  // The producer stages its slice's table rows (and slots) once the plan
+  // below is known: bring the tables to L2 while the plan reads the lengths
+  // (one line per thread and step, the last element included; at most
+  // kPrefetchLines lines per block).
+  {
+    auto prefetch_range = [&](const void* base, int64_t bytes) {
+      const char* p = static_cast<const char*>(base);
+      for (int64_t off = static_cast<int64_t>(threadIdx.x) * 128;
+           off < bytes && off < kPrefetchLines * 128ll; off += kDecodeThreads * 128ll)
+        prefetch_l2(p + off);
+      if (threadIdx.x == 0 && bytes > 0) prefetch_l2(p + bytes - 4);
+    };
+    prefetch_range(a.block_tables, static_cast<int64_t>(a.num_seqs) * a.max_blocks * 4);
+    if (a.slot_mapping != nullptr) prefetch_range(a.slot_mapping, static_cast<int64_t>(a.num_seqs) * 4);
+  }
+
   const int max_ctx = a.max_blocks * kBlockSize;
   const int hkv = a.num_kv_heads;
 
@@ -783,19 +800,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       auto emit_piece = [&](int pseq, int pctx, bool pbad_ctx, int pnch, int kvh, int k0, int n,
                             long long pfirst, long long pstart, int slot) -> bool {
         const bool whole = k0 == 0 && n == pnch;
-        // The blocks holding the pair's first and last chunk, and the partial
-        // slot of its piece in the first: the cross-block merge's bookkeeping,
-        // needed only for a cut pair (a whole pair's output is written by the
-        // merger directly).  The piece is that block's first (slot 0) when
-        // its slice holds no chunk of an earlier pair: it starts at or after
-        // the pair's first cost unit (every unit before that, back to the
-        // previous pair's gap, is a chunk of the previous pair).
+        // A cut pair's merge bookkeeping (below): computed once the piece's
+        // first copies are on their way, since its divisions are slow and the
+        // consumers read it only at the piece's end.
         int c_first = static_cast<int>(blockIdx.x), c_last = c_first, first_slot = 0;
-        if (!whole) {
-          c_first = block_of_chunk(pfirst, T, nb);
-          c_last = block_of_chunk(pfirst + pnch - 1, T, nb);
-          first_slot = slice_begin(c_first, T, nb) >= pstart ? 0 : 1;
-        }
         const int32_t* table = a.block_tables + static_cast<int64_t>(pseq) * a.max_blocks;
         const int32_t* stab = tab_smem ? sm.slice_tab + (pseq - tab_seq0) * a.max_blocks : table;
         for (int k = k0; k < k0 + n; ++k, ++c) {
@@ -812,41 +820,28 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
               report_error(a.err, kErrDeviceCheck, kSiteDecodeBlock);
             }
           }
-          // The descriptor is built in registers and stored once.
-          StageInfo inf;
-          inf.seq = pseq;
-          inf.kvh = kvh;
-          inf.slot = slot;
-          inf.n_valid = bad ? 0 : n_valid;
-          inf.flags = (bad ? kBad : 0) | (whole ? kSingle : 0) | (k == k0 ? kFirst : 0) |
-                      (k == k0 + n - 1 ? kLast : 0);
-          inf.c_first = c_first;
-          inf.c_last = c_last;
-          inf.first_slot = first_slot;
-          inf.store_slot = -1;
-          inf.store_row = 0;
-          inf.pad[0] = inf.pad[1] = 0;
+          const int valid = bad ? 0 : n_valid;
           const int slot_row = id * kBlockSize + (tok & (kBlockSize - 1));
+          int store_slot = -1, store_row = 0;
           if (fused && k == pnch - 1) {
             // The pair's last chunk holds the new token (position ctx - 1).
             const int want = slot_smem ? sm.slice_slot[pseq - tab_seq0] : a.slot_mapping[pseq];
-            if (inf.n_valid > 0 && want == slot_row + inf.n_valid - 1) {
-              inf.store_slot = want;
-              inf.store_row = inf.n_valid - 1;
+            if (valid > 0 && want == slot_row + valid - 1) {
+              store_slot = want;
+              store_row = valid - 1;
             } else if (want != -1) {
               report_error(a.err, kErrDeviceCheck, kSiteDecodeStoreSlot);
             }
           }
-          sm.info[st] = inf;
+          // The copies go first: the barrier is told their bytes, and its
+          // phase cannot complete before the arrive below, which publishes
+          // the descriptor written after them.
           const uint32_t fb = smem_u32(&sm.full[st]);
-          if (inf.n_valid <= 0) {
-            mbar_arrive(fb);  // descriptor only
-          } else {
+          if (valid > 0) {
             constexpr uint32_t kRowBytes = D * 2;
             constexpr uint32_t kScaleBytes = kI8 ? kChunk * 4 : 0u;
-            mbar_arrive_expect_tx(fb, 2 * kChunkBytes + 2 * kScaleBytes +
-                                          (k == k0 ? kQBytes : 0u) +
-                                          (inf.store_slot >= 0 ? 2 * kRowBytes : 0u));
+            mbar_expect_tx(fb, 2 * kChunkBytes + 2 * kScaleBytes + (k == k0 ? kQBytes : 0u) +
+                                   (store_slot >= 0 ? 2 * kRowBytes : 0u));
             if constexpr (kI8) {
               // Head-major INT8 blocks: the chunk's codes of this KV head are
               // one contiguous 64 x D tile (rows of (block, head) = id * Hkv
@@ -871,7 +866,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                             static_cast<int64_t>(pseq) * a.q_row_stride +
                             static_cast<int64_t>(kvh) * G * D,
                         kQBytes, fb);
-            if (inf.store_slot >= 0) {
+            if (store_slot >= 0) {
               bulk_load(smem_u32(&sm.knew[st][0]),
                         static_cast<const __nv_bfloat16*>(a.k_new) +
                             static_cast<int64_t>(pseq) * a.k_new_stride +
@@ -884,6 +879,35 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                         kRowBytes, fb);
             }
           }
+          if (k == k0 && !whole) {
+            // The blocks holding the pair's first and last chunk, and the
+            // partial slot of its piece in the first: the cross-block merge's
+            // bookkeeping, needed only for a cut pair (a whole pair's output
+            // is written by the merger directly).  The piece is that block's
+            // first (slot 0) when its slice holds no chunk of an earlier pair:
+            // it starts at or after the pair's first cost unit (every unit
+            // before that, back to the previous pair's gap, is a chunk of the
+            // previous pair).
+            c_first = block_of_chunk(pfirst, T, nb);
+            c_last = block_of_chunk(pfirst + pnch - 1, T, nb);
+            first_slot = slice_begin(c_first, T, nb) >= pstart ? 0 : 1;
+          }
+          // The descriptor is built in registers and stored once.
+          StageInfo inf;
+          inf.seq = pseq;
+          inf.kvh = kvh;
+          inf.slot = slot;
+          inf.n_valid = valid;
+          inf.flags = (bad ? kBad : 0) | (whole ? kSingle : 0) | (k == k0 ? kFirst : 0) |
+                      (k == k0 + n - 1 ? kLast : 0);
+          inf.c_first = c_first;
+          inf.c_last = c_last;
+          inf.first_slot = first_slot;
+          inf.store_slot = store_slot;
+          inf.store_row = store_row;
+          inf.pad[0] = inf.pad[1] = 0;
+          sm.info[st] = inf;
+          mbar_arrive(fb);
         }
         return true;
       };
