@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 }
 TRAFFIC_CAPTURES = {
     # kernel: (sha256 of its sources, workload, dram bytes per launch)
-    "decode_append": ("5218d014c6d1d98c28dd3248c79cbb12ce3f2e97773255e85ecb4e46773faff8", MAIN_WORKLOAD,
-                      324845312 + 4020736),
+    "decode_append": ("c50eda2520f3cade45e0bb2510ec34cc8665aead7cf845c126939f89758649f2", MAIN_WORKLOAD,
+                      324840192 + 4035072),
 }
 
 
